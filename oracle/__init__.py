@@ -1,0 +1,252 @@
+"""CPU oracle for SIFT's online prefill hot path -- test infrastructure only.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+(and its ``--impl reference`` arm) import this package.  The product path
+(``bit_vector_guided_gb300``) never does, and the two share no code: the only
+common dependency is the seeded input generator in ``workloads``.
+
+Two independent restatements of the same definition live here:
+  * ``sift_oracle.c`` (built by :func:`build`): row-by-row masked softmax
+    attention whose key set is read straight from the LA/CA bits, plus a
+    plain nested-loop bit decode;
+  * :func:`brute_force_attention` (numpy, fp64): a tile-level mask is expanded
+    to an explicit token mask and dense softmax attention is taken with
+    ``-inf`` outside it -- only for tiny inputs.
+
+See ``sift_oracle.c`` for the readings of the pages (gist.science/it/paper/
+2606.09441, "Design del Sistema", "Dettagli di Implementazione") and the pins.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "sift_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libsift_oracle.so")
+_lib = None
+
+__all__ = ["build", "load", "decode", "schedule", "attention_rows", "attention_all",
+           "key_mask", "brute_force_attention", "tile_mask", "set_threads"]
+
+
+def build(force: bool = False) -> str:
+    """Compile sift_oracle.c with gcc (-O2 -fopenmp) into oracle/_build/."""
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.sift_oracle_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, P, P]
+        lib.sift_oracle_decode.restype = i32
+        lib.sift_oracle_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32,
+                                                   i32, i32, f64, P, P, P, i64, P, P, P, P]
+        lib.sift_oracle_attention_rows.restype = i32
+        lib.sift_oracle_key_mask.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
+                                             i64, P, i64, P, P]
+        lib.sift_oracle_key_mask.restype = i32
+        lib.sift_oracle_set_threads.argtypes = [i32]
+        lib.sift_oracle_set_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+def set_threads(n: int = 0) -> int:
+    """Set (n > 0) and return the number of OpenMP threads the oracle uses."""
+    return int(load().sift_oracle_set_threads(int(n)))
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _layout_args(layout, la_words, ca_words):
+    arrs = [np.ascontiguousarray(layout.cu_seqlens, np.int32),
+            np.ascontiguousarray(layout.doc_cu, np.int32),
+            np.ascontiguousarray(layout.doc_end, np.int32),
+            np.ascontiguousarray(layout.la_off, np.int64),
+            np.ascontiguousarray(layout.ca_off, np.int64),
+            np.ascontiguousarray(la_words, np.uint64) if len(la_words) else np.zeros(1, np.uint64),
+            np.ascontiguousarray(ca_words, np.uint64) if len(ca_words) else np.zeros(1, np.uint64)]
+    if len(arrs[2]) == 0:
+        arrs[2] = np.zeros(1, np.int32)
+        arrs[3] = np.zeros(1, np.int64)
+        arrs[4] = np.zeros(1, np.int64)
+    return arrs
+
+
+def decode(layout, la_words, ca_words, rowcap: Optional[int] = None):
+    """Tile index lists of every (layer, kv head, query tile) row.
+
+    Returns (kv_idx int32 [L, Hkv, N, rowcap] with -1 padding, counts int32 [L, Hkv, N]).
+    """
+    lib = load()
+    rowcap = rowcap or layout.max_tiles_per_prompt
+    L, Hkv, N = layout.num_layers, layout.num_kv_heads, layout.num_tiles
+    kv_idx = np.full((L, Hkv, N, rowcap), -1, np.int32)
+    counts = np.zeros((L, Hkv, N), np.int32)
+    arrs = _layout_args(layout, la_words, ca_words)
+    rc = lib.sift_oracle_decode(layout.num_prompts, layout.num_docs, L, Hkv, layout.tile,
+                                *[_ptr(a) for a in arrs], rowcap, _ptr(kv_idx), _ptr(counts))
+    if rc != 0:
+        raise ValueError("oracle decode: a row exceeds rowcap")
+    return kv_idx, counts
+
+
+def schedule(counts: np.ndarray) -> np.ndarray:
+    """Longest-first order of the (kv head, query tile) units of each layer.
+
+    counts [L, Hkv, N] -> sched [L, Hkv*N] with unit index u = h*N + i, sorted by
+    count descending, ties by u ascending.  Any order with non-increasing counts is
+    an equally valid schedule; this one is the unique stable representative.
+    """
+    L = counts.shape[0]
+    flat = counts.reshape(L, -1)
+    return np.stack([np.argsort(-flat[l], kind="stable") for l in range(L)]).astype(np.int32)
+
+
+def _bf16_bits(x) -> np.ndarray:
+    """torch bf16 tensor (any device) or uint16 array -> contiguous uint16 numpy."""
+    if isinstance(x, np.ndarray):
+        return np.ascontiguousarray(x, np.uint16)
+    import torch
+    return np.ascontiguousarray(x.detach().to("cpu").contiguous().view(torch.int16).numpy()
+                                .view(np.uint16))
+
+
+def attention_rows(layout, la_words, ca_words, layer, q, k, v, row_tok, row_head,
+                   scale: Optional[float] = None):
+    """O (fp64 [n, d]) and LSE (fp64 [n]) for the requested (token, query head) rows."""
+    lib = load()
+    d = layout.head_dim
+    scale = (1.0 / np.sqrt(d)) if scale is None else float(scale)
+    qb, kb, vb = _bf16_bits(q), _bf16_bits(k), _bf16_bits(v)
+    row_tok = np.ascontiguousarray(row_tok, np.int32)
+    row_head = np.ascontiguousarray(row_head, np.int32)
+    n = len(row_tok)
+    out_o = np.zeros((max(n, 1), d), np.float64)
+    out_lse = np.zeros(max(n, 1), np.float64)
+    arrs = _layout_args(layout, la_words, ca_words)
+    rc = lib.sift_oracle_attention_rows(
+        layout.num_prompts, layout.num_docs, layout.num_kv_heads, layout.tile,
+        *[_ptr(a) for a in arrs], int(layer), layout.num_q_heads, d, scale,
+        _ptr(qb), _ptr(kb), _ptr(vb), n, _ptr(row_tok), _ptr(row_head),
+        _ptr(out_o), _ptr(out_lse))
+    if rc != 0:
+        raise ValueError("oracle attention: row outside the batch")
+    return out_o[:n], out_lse[:n]
+
+
+def attention_all(layout, la_words, ca_words, layer, q, k, v, scale=None):
+    """Every row of one layer: O fp64 [tokens, Hq, d], LSE fp64 [Hq, tokens]."""
+    T, Hq, d = layout.total_tokens, layout.num_q_heads, layout.head_dim
+    tok = np.repeat(np.arange(T, dtype=np.int32), Hq)
+    head = np.tile(np.arange(Hq, dtype=np.int32), T)
+    o, lse = attention_rows(layout, la_words, ca_words, layer, q, k, v, tok, head, scale)
+    return o.reshape(T, Hq, d), lse.reshape(T, Hq).T.copy()
+
+
+def key_mask(layout, la_words, ca_words, layer, kv_head, q_tok, k_tok) -> np.ndarray:
+    """0/1 [len(q_tok), len(k_tok)] visibility matrix from the bits (same rule as attention_rows)."""
+    lib = load()
+    q_tok = np.ascontiguousarray(q_tok, np.int32)
+    k_tok = np.ascontiguousarray(k_tok, np.int32)
+    out = np.zeros((len(q_tok), len(k_tok)), np.uint8)
+    arrs = _layout_args(layout, la_words, ca_words)
+    lib.sift_oracle_key_mask(layout.num_prompts, layout.num_docs, layout.num_kv_heads,
+                             layout.tile, *[_ptr(a) for a in arrs], int(layer), int(kv_head),
+                             len(q_tok), _ptr(q_tok), len(k_tok), _ptr(k_tok), _ptr(out))
+    return out.astype(bool)
+
+
+# --------------------------------------------------------------------------------------
+# Second, independent restatement for tiny inputs: explicit dense masks in numpy.
+# --------------------------------------------------------------------------------------
+
+def _unpack(words: np.ndarray, nbits: int) -> np.ndarray:
+    """uint64 words [..., W] -> bool [..., nbits], bit j = bit (j%64) of word j//64."""
+    by = np.ascontiguousarray(words, "<u8").view(np.uint8)
+    bits = np.unpackbits(by.reshape(words.shape[:-1] + (-1,)), axis=-1, bitorder="little")
+    return bits[..., :nbits].astype(bool)
+
+
+def tile_mask(layout, la_words, ca_words, layer, kv_head) -> np.ndarray:
+    """Global tile-level mask M[i, j] (query tile i may use key tile j).
+
+    Built block by block from the plain description: a prompt's tiles see only
+    tiles of the same prompt; suffix rows see every tile up to the diagonal;
+    document rows see the diagonal, the LA-flagged tiles below it inside the
+    document, and the CA-flagged pages of every earlier document.
+    """
+    B, Hkv = layout.tile, layout.num_kv_heads
+    N = layout.num_tiles
+    M = np.zeros((N, N), bool)
+    for p in range(layout.num_prompts):
+        t0, t1 = layout.cu_seqlens[p] // B, layout.cu_seqlens[p + 1] // B
+        docs = range(layout.doc_cu[p], layout.doc_cu[p + 1])
+        spans = []
+        for g in docs:
+            s = layout.doc_start(g) // B
+            T = layout.doc_tiles(g)
+            W = (T + 63) // 64
+            base = layout.la_off[g] + (layer * Hkv + kv_head) * T * W
+            la = _unpack(la_words[base: base + T * W].reshape(T, W), T)
+            cbase = layout.ca_off[g] + (layer * Hkv + kv_head) * W
+            ca = _unpack(ca_words[cbase: cbase + W].reshape(1, W), T)[0]
+            spans.append((s, T, la, ca))
+        for k, (s, T, la, ca) in enumerate(spans):
+            M[s:s + T, s:s + T] |= np.tril(la, -1)
+            for (s2, T2, _, ca2) in spans[:k]:
+                M[s:s + T, s2:s2 + T2] |= ca2[None, :]
+        last = spans[-1][0] + spans[-1][1] if spans else t0
+        for i in range(last, t1):
+            M[i, t0:i + 1] = True
+        for i in range(t0, t1):
+            M[i, i] = True
+    return M
+
+
+def brute_force_attention(layout, la_words, ca_words, layer, q, k, v, scale=None):
+    """Dense fp64 attention with -inf outside the expanded token mask (tiny inputs only)."""
+    qb = _bf16_bits(q).astype(np.uint32) << 16
+    kb = _bf16_bits(k).astype(np.uint32) << 16
+    vb = _bf16_bits(v).astype(np.uint32) << 16
+    qf = qb.view(np.float32).astype(np.float64)
+    kf = kb.view(np.float32).astype(np.float64)
+    vf = vb.view(np.float32).astype(np.float64)
+    T, Hq, d = qf.shape
+    Hkv = kf.shape[1]
+    G = Hq // Hkv
+    B = layout.tile
+    scale = (1.0 / np.sqrt(d)) if scale is None else float(scale)
+    causal = np.tril(np.ones((T, T), bool))
+    O = np.zeros((T, Hq, d))
+    LSE = np.zeros((Hq, T))
+    for h in range(Hkv):
+        M = np.kron(tile_mask(layout, la_words, ca_words, layer, h),
+                    np.ones((B, B), bool)) & causal
+        for qh in range(h * G, (h + 1) * G):
+            S = scale * qf[:, qh, :] @ kf[:, h, :].T
+            S = np.where(M, S, -np.inf)
+            m = S.max(axis=1, keepdims=True)
+            P = np.exp(S - m)
+            l = P.sum(axis=1, keepdims=True)
+            O[:, qh, :] = (P / l) @ vf[:, h, :]
+            LSE[qh] = (m + np.log(l))[:, 0]
+    return O, LSE
