@@ -1,0 +1,15 @@
+"""SIFT online-prefill hot path for GB300 (sm_103a).
+
+``sift_decode`` (bits -> tile lists + longest-first schedule),
+``sift_sparse_prefill`` (block-sparse causal GQA flash attention) and
+``sift_dense_prefill`` (the dense full-recompute baseline) live in the CUDA
+library ``libsift.so`` behind the C ABI of ``include/sift.h``; this package is
+the Python binding of that library.
+"""
+from ._native import (STATUS, SiftError, SiftProblem, abi_version, debug_set_waits, decode,
+                      dense_prefill, exported_symbols, load_library, sparse_prefill,
+                      status_string, workspace_bytes)
+
+__all__ = ["STATUS", "SiftError", "SiftProblem", "abi_version", "debug_set_waits", "decode",
+           "dense_prefill", "exported_symbols", "load_library", "sparse_prefill", "status_string",
+           "workspace_bytes"]

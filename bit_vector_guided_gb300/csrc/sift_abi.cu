@@ -1,0 +1,80 @@
+// sift_abi.cu -- status strings, argument validation, workspace sizing and the
+// wait-limit test hook of the C ABI declared in include/sift.h.
+#include <atomic>
+#include <climits>
+
+#include "sift_internal.h"
+
+namespace sift {
+
+static std::atomic<uint64_t> g_timeout_ns{kDefaultWaitTimeoutNs};
+static std::atomic<int32_t> g_stall{0};
+
+DebugWaits debug_waits() { return DebugWaits{g_timeout_ns.load(), g_stall.load()}; }
+
+sift_status validate_problem(const sift_problem *p, bool attention) {
+    if (p == nullptr) return SIFT_ERR_INVALID_ARG;
+    if (p->num_prompts < 1 || p->num_docs < 0 || p->num_layers < 1 || p->num_q_heads < 1 ||
+        p->num_kv_heads < 1 || p->tile < 1 || p->total_tokens < 1 ||
+        p->max_tiles_per_prompt < 1 || p->la_words_len < 0 || p->ca_words_len < 0)
+        return SIFT_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return SIFT_ERR_INVALID_ARG;
+    if (p->total_tokens % p->tile != 0) return SIFT_ERR_UNSUPPORTED;
+    if (p->cu_seqlens == nullptr || p->doc_cu == nullptr) return SIFT_ERR_INVALID_ARG;
+    if (p->num_docs > 0 && (p->doc_end == nullptr || p->la_off == nullptr || p->ca_off == nullptr))
+        return SIFT_ERR_INVALID_ARG;
+    const int64_t N = p->total_tokens / p->tile;
+    if (N * p->num_kv_heads > INT32_MAX / 2) return SIFT_ERR_UNSUPPORTED;
+    if (p->max_tiles_per_prompt > N || p->max_tiles_per_prompt > 49152)
+        return SIFT_ERR_INVALID_ARG;
+    if (attention) {
+        if (p->head_dim != 64 && p->head_dim != 128) return SIFT_ERR_UNSUPPORTED;
+        if (p->tile != 64 && p->tile != 128) return SIFT_ERR_UNSUPPORTED;
+        if ((p->num_q_heads / p->num_kv_heads) % 2 != 0) return SIFT_ERR_UNSUPPORTED;
+        if (static_cast<int64_t>(p->total_tokens) * p->num_q_heads * p->head_dim > INT32_MAX * 8ll)
+            return SIFT_ERR_UNSUPPORTED;
+    }
+    return SIFT_OK;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < 64) cache[dev] = n;
+    return n;
+}
+
+}  // namespace sift
+
+extern "C" {
+
+const char *sift_status_string(sift_status s) {
+    switch (s) {
+        case SIFT_OK: return "SIFT_OK";
+        case SIFT_ERR_INVALID_ARG: return "SIFT_ERR_INVALID_ARG";
+        case SIFT_ERR_UNSUPPORTED: return "SIFT_ERR_UNSUPPORTED";
+        case SIFT_ERR_CUDA: return "SIFT_ERR_CUDA";
+        case SIFT_ERR_TIMEOUT: return "SIFT_ERR_TIMEOUT";
+        case SIFT_ERR_DEVICE_CHECK: return "SIFT_ERR_DEVICE_CHECK";
+    }
+    return "SIFT_ERR_UNKNOWN";
+}
+
+size_t sift_workspace_bytes(const sift_problem *p) {
+    if (sift::validate_problem(p, false) != SIFT_OK) return 0;
+    const size_t units = static_cast<size_t>(p->total_tokens / p->tile) * p->num_kv_heads;
+    return sift::kWsHeader + 2 * units * sizeof(int32_t);
+}
+
+void sift_debug_set_waits(uint64_t wait_timeout_ns, int32_t stall_flag) {
+    sift::g_timeout_ns.store(wait_timeout_ns ? wait_timeout_ns : sift::kDefaultWaitTimeoutNs);
+    sift::g_stall.store(stall_flag);
+}
+
+int32_t sift_abi_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,653 @@
+// sift_attention.cu -- block-sparse (and dense) causal grouped-query flash
+// attention for SIFT's online prefill on sm_103a.
+//
+// SIFT pages (gist.science/it/paper/2606.09441), "Dettagli di
+// Implementazione": the sparse attention kernel iterates only over the tile
+// indices decoded from the bit vectors; "Esecuzione Online": flagged tiles are
+// computed, the rest skipped.  The pages' kernel extends FlashAttention-3 on
+// H200; this one is written for Blackwell: TMA tile loads, tcgen05 MMAs with
+// the accumulators in tensor memory, and a persistent longest-first scheduler.
+//
+// One work item = (query tile i, kv head h, pair of query heads of h's group).
+// Both heads of the pair share every K/V tile staged in shared memory, and the
+// decoded list of row (h, i).  Roles inside the 320-thread CTA:
+//   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax of head slot 1
+//   warp  8    scheduler + TMA producer (Q pair, then K_j, V_j into a 4-stage ring)
+//   warp  9    TMEM allocator + single-thread MMA issuer
+// Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
+// each.  P (bf16, two per column) overwrites the first half of its S, and the
+// P*V MMA reads it from tensor memory, so P never touches shared memory.
+// MMA order per item: S0(0) S1(0) | PV0(0) S0(1) | PV1(0) S1(1) | ... so the
+// tensor pipe works on one head while the other head's softmax runs.
+// Online softmax keeps a per-row running max m (log2 units) and sum l; O is
+// rescaled only when m grows by more than 8 (factor 256) -- otherwise the
+// stale max is kept, which stays exact because O and l share it.
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
+// SIFT_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <climits>
+#include <mutex>
+
+#include "ptx.cuh"
+#include "sift_internal.h"
+
+namespace sift {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kStages = 4;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kFull = 0xffffffffu;
+constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all of TMEM)
+
+struct WorkItem {
+    int32_t valid;
+    int32_t h;      // kv head
+    int32_t i;      // global query tile
+    int32_t hq0;    // first query head of the pair
+    int32_t n;      // key tiles in the row's list
+    int32_t first;  // dense rows: first tile of the prompt
+    int64_t list;   // sparse rows: element offset of the row inside the kv_idx slice
+};
+
+struct Ctl {
+    uint64_t q_full, q_empty;
+    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t s_full[2], p_full[2], o_full[2];
+    uint64_t sch_full[2], sch_empty[2];
+    uint64_t teardown, never;
+    WorkItem items[2];
+    uint32_t tmem_base;
+    volatile int32_t abort;
+};
+
+struct AttnParams {
+    const int32_t *kv_idx;  // layer slice [Hkv][N][rowcap] (sparse)
+    const int32_t *counts;  // [U]
+    const int32_t *sched;   // [U]
+    __nv_bfloat16 *o;
+    float *lse;
+    int32_t *work_counter;
+    int32_t *status;
+    int32_t total_items, U, N, Hq, G, pairs, rowcap, total_tokens;
+    float scale_log2;
+    uint64_t timeout_ns;
+    int32_t stall;
+};
+
+template <int BT, int HD>
+struct Geo {
+    static constexpr int kBoxes = HD / 64;          // 64-column (128-byte) swizzled boxes
+    static constexpr int kQBox = 128 * 128;          // bytes: 128 rows (MMA M) x 128 B
+    static constexpr int kQBytes = 2 * kBoxes * kQBox;
+    static constexpr int kKVBox = BT * 128;
+    static constexpr int kKVBytes = kBoxes * kKVBox;
+    static constexpr int kRingOff = kQBytes;
+    static constexpr int kCtlOff = kQBytes + kStages * kKVBytes;
+    static constexpr int kSmemUsed = kCtlOff + 1024 + 1024;  // + control block + align slack
+    static constexpr int kSmem = kSmemUsed > kMinSmem ? kSmemUsed : kMinSmem;
+    static constexpr uint32_t kTxQ = 2 * kBoxes * BT * 128;
+    static constexpr uint32_t kTxKV = kBoxes * BT * 128;
+    static constexpr int kSoftWarps = BT / 32;       // active softmax warps per head slot
+    static constexpr uint32_t kIdescS = ptx::idesc_bf16(128, BT, false, false);
+    static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, HD, false, true);
+    static_assert(sizeof(Ctl) <= 1024, "control block");
+    static_assert(kSmemUsed <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ void set_status(int32_t *st, int code) { atomicCAS(st, 0, code); }
+
+// bounded wait; gives up early once another role has aborted
+__device__ __noinline__ bool wait_bar(Ctl &c, uint32_t bar, uint32_t parity, uint64_t timeout,
+                                      int32_t *status) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (c.abort) return false;
+        if (ptx::globaltimer_ns() - t0 > timeout) {
+            c.abort = 1;
+            set_status(status, SIFT_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// bounded wait used while unwinding (ignores the abort flag)
+__device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, uint64_t timeout) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer_ns() - t0 > timeout) return false;
+    return true;
+}
+
+// all lanes wait, result made warp-uniform
+__device__ __forceinline__ bool wait_warp(Ctl &c, uint32_t bar, uint32_t parity,
+                                          const AttnParams &p) {
+    const bool ok = wait_bar(c, bar, parity, p.timeout_ns, p.status);
+    return __all_sync(kFull, ok);
+}
+
+template <bool DENSE>
+__device__ __forceinline__ WorkItem fetch_item(const AttnParams &p, int w) {
+    WorkItem it{};
+    if (w >= p.total_items) return it;
+    const int uidx = w / p.pairs;
+    const int pair = w - uidx * p.pairs;
+    int unit = __ldg(p.sched + uidx);
+    if (unit < 0 || unit >= p.U) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        unit = uidx;
+    }
+    it.h = unit / p.N;
+    it.i = unit - it.h * p.N;
+    it.hq0 = it.h * p.G + 2 * pair;
+    int n = __ldg(p.counts + unit);
+    const int nmax = DENSE ? it.i + 1 : p.rowcap;
+    if (n < 1 || n > nmax) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        n = n < 1 ? 1 : nmax;
+    }
+    it.n = n;
+    it.first = it.i - n + 1;
+    it.list = (static_cast<int64_t>(it.h) * p.N + it.i) * p.rowcap;
+    it.valid = 1;
+    return it;
+}
+
+template <int BT, int HD, bool DENSE>
+__global__ void __launch_bounds__(kThreads, 1)
+sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
+                      const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+    using G = Geo<BT, HD>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    const uint32_t q_s = sbase;
+    const uint32_t ring_s = sbase + G::kRingOff;
+    Ctl &c = *reinterpret_cast<Ctl *>(smem + G::kCtlOff);
+
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31u;
+
+    auto B_ = [&](const uint64_t &b) { return ptx::smem_u32(&b); };
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(B_(c.q_full), 1);
+        ptx::mbar_init(B_(c.q_empty), 1);
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(B_(c.kv_full[s]), 1);
+            ptx::mbar_init(B_(c.kv_empty[s]), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(B_(c.s_full[s]), 1);
+            ptx::mbar_init(B_(c.p_full[s]), G::kSoftWarps);
+            ptx::mbar_init(B_(c.o_full[s]), 1);
+            ptx::mbar_init(B_(c.sch_full[s]), 1);
+            ptx::mbar_init(B_(c.sch_empty[s]), 1 + 2 * G::kSoftWarps);
+        }
+        ptx::mbar_init(B_(c.teardown), 1);
+        ptx::mbar_init(B_(c.never), 1);
+        c.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == kProducerWarp && lane == 0) {
+        ptx::prefetch_tmap(&tmQ);
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
+    }
+    if (warp == kMmaWarp) {
+        ptx::tmem_alloc(ptx::smem_u32(&c.tmem_base), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = c.tmem_base;
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------ scheduler + TMA producer
+        int item_k = 0, qk = 0, f = 0;
+        bool alive = true;
+        while (alive) {
+            int w = 0;
+            if (lane == 0) w = atomicAdd(p.work_counter, 1);
+            w = __shfl_sync(kFull, w, 0);
+            const WorkItem it = fetch_item<DENSE>(p, w);
+            const int slot = item_k & 1;
+            if (!wait_warp(c, B_(c.sch_empty[slot]), ((item_k >> 1) & 1) ^ 1, p)) break;
+            if (lane == 0) {
+                c.items[slot] = it;
+                ptx::mbar_arrive(B_(c.sch_full[slot]));
+            }
+            __syncwarp();
+            ++item_k;
+            if (!it.valid) break;
+            if (!wait_warp(c, B_(c.q_empty), (qk & 1) ^ 1, p)) break;
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(B_(c.q_full), G::kTxQ);
+                for (int s = 0; s < 2; ++s)
+                    for (int b = 0; b < G::kBoxes; ++b)
+                        ptx::tma_load_3d(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ, B_(c.q_full),
+                                         64 * b, it.hq0 + s, it.i * BT);
+            }
+            ++qk;
+            for (int jb = 0; jb < it.n && alive; jb += 32) {
+                const int j = jb + static_cast<int>(lane);
+                int my = 0;
+                if (j < it.n) {
+                    if (DENSE) {
+                        my = it.first + j;
+                    } else {
+                        my = __ldg(p.kv_idx + it.list + j);
+                        const bool bad = my < 0 || my > it.i || (j == it.n - 1 && my != it.i);
+                        if (bad) {
+                            set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+                            my = it.i;
+                        }
+                    }
+                }
+                const int cnt = min(32, it.n - jb);
+                for (int jj = 0; jj < cnt; ++jj) {
+                    const int idx = __shfl_sync(kFull, my, jj);
+                    for (int kind = 0; kind < 2; ++kind) {
+                        const int slot2 = f % kStages;
+                        if (!wait_warp(c, B_(c.kv_empty[slot2]), ((f / kStages) & 1) ^ 1, p)) {
+                            alive = false;
+                            break;
+                        }
+                        if (lane == 0) {
+                            ptx::mbar_arrive_expect_tx(B_(c.kv_full[slot2]), G::kTxKV);
+                            const uint32_t dst = ring_s + slot2 * G::kKVBytes;
+                            for (int b = 0; b < G::kBoxes; ++b)
+                                ptx::tma_load_3d(dst + b * G::kKVBox, kind ? &tmV : &tmK,
+                                                 B_(c.kv_full[slot2]), 64 * b, it.h, idx * BT);
+                        }
+                        ++f;
+                    }
+                    if (!alive) break;
+                }
+            }
+        }
+        if (c.abort && lane == 0) {
+            // unwinding: let every copy already issued land before shared memory is released
+            for (int s = 0; s < kStages && s < f; ++s) {
+                const int last = s + ((f - 1 - s) / kStages) * kStages;  // last fill of slot s
+                drain_bar(B_(c.kv_full[s]), (last / kStages) & 1, p.timeout_ns);
+            }
+            if (qk > 0) drain_bar(B_(c.q_full), (qk - 1) & 1, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------ single-thread MMA issuer
+        if (lane == 0) {
+            if (p.stall) wait_bar(c, B_(c.never), 0, p.timeout_ns, p.status);
+            int item_k = 0, qk = 0, f = 0;
+            uint32_t pph0 = 0, pph1 = 0;
+            const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+            auto issue_s = [&](int s, int slot) {
+                const uint32_t qa = q_s + s * G::kBoxes * G::kQBox;
+                const uint32_t kb = ring_s + slot * G::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t off_q = (kk >> 2) * G::kQBox + (kk & 3) * 32;
+                    const uint32_t off_k = (kk >> 2) * G::kKVBox + (kk & 3) * 32;
+                    ptx::umma_ss(s ? tS1 : tS0, ptx::sdesc_sw128(qa + off_q, 16, 1024),
+                                 ptx::sdesc_sw128(kb + off_k, 16, 1024), G::kIdescS, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int s, int slot, bool acc) {
+                const uint32_t vb = ring_s + slot * G::kKVBytes;
+#pragma unroll
+                for (int kk = 0; kk < BT / 16; ++kk) {
+                    ptx::umma_ts(s ? tO1 : tO0, (s ? tS1 : tS0) + kk * 8,
+                                 ptx::sdesc_sw128(vb + kk * 16 * 128, G::kKVBox, 1024),
+                                 G::kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            while (!c.abort) {
+                const int slot = item_k & 1;
+                if (!wait_bar(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p.timeout_ns, p.status))
+                    break;
+                const WorkItem it = c.items[slot];
+                ptx::mbar_arrive(B_(c.sch_empty[slot]));
+                ++item_k;
+                if (!it.valid) break;
+                if (!wait_bar(c, B_(c.q_full), qk & 1, p.timeout_ns, p.status)) break;
+                ++qk;
+                ptx::tc_fence_after();
+                bool ok = true;
+                int fVp = 0;
+                for (int j = 0; j < it.n; ++j) {
+                    const int fK = f, fV = f + 1;
+                    f += 2;
+                    if (!wait_bar(c, B_(c.kv_full[fK % kStages]), (fK / kStages) & 1,
+                                  p.timeout_ns, p.status)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    if (j > 0) {
+                        if (!wait_bar(c, B_(c.kv_full[fVp % kStages]), (fVp / kStages) & 1,
+                                      p.timeout_ns, p.status)) { ok = false; break; }
+                        if (!wait_bar(c, B_(c.p_full[0]), pph0, p.timeout_ns, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        pph0 ^= 1;
+                        ptx::tc_fence_after();
+                        issue_pv(0, fVp % kStages, j > 1);
+                    }
+                    issue_s(0, fK % kStages);
+                    ptx::umma_commit(B_(c.s_full[0]));
+                    if (j > 0) {
+                        if (!wait_bar(c, B_(c.p_full[1]), pph1, p.timeout_ns, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        pph1 ^= 1;
+                        ptx::tc_fence_after();
+                        issue_pv(1, fVp % kStages, j > 1);
+                        ptx::umma_commit(B_(c.kv_empty[fVp % kStages]));
+                    }
+                    issue_s(1, fK % kStages);
+                    ptx::umma_commit(B_(c.s_full[1]));
+                    ptx::umma_commit(B_(c.kv_empty[fK % kStages]));
+                    if (j == it.n - 1) ptx::umma_commit(B_(c.q_empty));
+                    fVp = fV;
+                }
+                if (!ok) break;
+                if (!wait_bar(c, B_(c.kv_full[fVp % kStages]), (fVp / kStages) & 1, p.timeout_ns,
+                              p.status)) break;
+                if (!wait_bar(c, B_(c.p_full[0]), pph0, p.timeout_ns, p.status)) break;
+                pph0 ^= 1;
+                ptx::tc_fence_after();
+                issue_pv(0, fVp % kStages, it.n > 1);
+                ptx::umma_commit(B_(c.o_full[0]));
+                if (!wait_bar(c, B_(c.p_full[1]), pph1, p.timeout_ns, p.status)) break;
+                pph1 ^= 1;
+                ptx::tc_fence_after();
+                issue_pv(1, fVp % kStages, it.n > 1);
+                ptx::umma_commit(B_(c.o_full[1]));
+                ptx::umma_commit(B_(c.kv_empty[fVp % kStages]));
+            }
+            // every MMA issued so far must finish before TMEM and shared memory go away
+            ptx::umma_commit(B_(c.teardown));
+            drain_bar(B_(c.teardown), 0, p.timeout_ns);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax + epilogue
+        const int s = warp >> 2;
+        const int wq = warp & 3;
+        if (wq < G::kSoftWarps) {
+            const int row = wq * 32 + static_cast<int>(lane);
+            const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+            const uint32_t tS = tmem + lane_off + s * 128;
+            const uint32_t tO = tmem + lane_off + 256 + s * 128;
+            const float sl2 = p.scale_log2;
+            int item_k = 0;
+            uint32_t sph = 0, oph = 0;
+            while (true) {
+                const int slot = item_k & 1;
+                if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
+                const WorkItem it = c.items[slot];
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(B_(c.sch_empty[slot]));
+                ++item_k;
+                if (!it.valid) break;
+                float m = -INFINITY, l = 0.f;
+                bool ok = true;
+                for (int j = 0; j < it.n; ++j) {
+                    if (!wait_warp(c, B_(c.s_full[s]), sph, p)) { ok = false; break; }
+                    sph ^= 1;
+                    ptx::tc_fence_after();
+                    float x[BT];
+#pragma unroll
+                    for (int cc = 0; cc < BT / 32; ++cc)
+                        ptx::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&x[cc * 32]));
+                    if (j == it.n - 1) {
+#pragma unroll
+                        for (int cidx = 0; cidx < BT; ++cidx)
+                            if (cidx > row) x[cidx] = -INFINITY;
+                    }
+                    float mx = x[0];
+#pragma unroll
+                    for (int cidx = 1; cidx < BT; ++cidx) mx = fmaxf(mx, x[cidx]);
+                    const float m_new = fmaxf(m, mx * sl2);
+                    const bool need = m_new > m + 8.0f;
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = ptx::ex2(m - m_new);
+                        m = m_new;
+                    }
+                    l *= alpha;
+                    const float mb = m;
+#pragma unroll
+                    for (int cc = 0; cc < BT / 32; ++cc) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) {
+                            const float p0 = ptx::ex2(fmaf(x[cc * 32 + 2 * t], sl2, -mb));
+                            const float p1 = ptx::ex2(fmaf(x[cc * 32 + 2 * t + 1], sl2, -mb));
+                            l += p0 + p1;
+                            pk[t] = ptx::pack_bf16x2(p0, p1);
+                        }
+                        ptx::tmem_st16(tS + cc * 16, pk);
+                    }
+                    if (j > 0 && __any_sync(kFull, need)) {
+#pragma unroll 1
+                        for (int cc = 0; cc < HD / 32; ++cc) {
+                            float ov[32];
+                            ptx::tmem_ld32(tO + cc * 32, ov);
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) ov[t] *= alpha;
+                            ptx::tmem_st32f(tO + cc * 32, ov);
+                        }
+                    }
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(B_(c.p_full[s]));
+                }
+                if (!ok) break;
+                if (!wait_warp(c, B_(c.o_full[s]), oph, p)) break;
+                oph ^= 1;
+                ptx::tc_fence_after();
+                const float inv = 1.f / l;
+                const int64_t tok = static_cast<int64_t>(it.i) * BT + row;
+                const int hq = it.hq0 + s;
+                uint4 *orow = reinterpret_cast<uint4 *>(p.o + (tok * p.Hq + hq) * HD);
+#pragma unroll 1
+                for (int cc = 0; cc < HD / 32; ++cc) {
+                    float ov[32];
+                    ptx::tmem_ld32(tO + cc * 32, ov);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        pk[t] = ptx::pack_bf16x2(ov[2 * t] * inv, ov[2 * t + 1] * inv);
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        orow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
+                                                       pk[4 * v4 + 3]);
+                }
+                p.lse[static_cast<int64_t>(hq) * p.total_tokens + tok] =
+                    (m + log2f(l)) * 0.69314718055994530942f;
+                ptx::tc_fence_before();
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// [tokens][heads][d] bf16 viewed as a 3-D tensor (d, heads, tokens); box 64 x 1 x rows
+bool make_map(CUtensorMap *m, const void *base, int d, int heads, int tokens, int rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (enc == nullptr) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(heads),
+                          static_cast<cuuint64_t>(tokens)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                             static_cast<cuuint64_t>(heads) * d * 2};
+    cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(rows)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+           CUDA_SUCCESS;
+}
+
+template <int BT, int HD, bool DENSE>
+sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
+                             const AttnParams &p, cudaStream_t stream) {
+    using G = Geo<BT, HD>;
+    auto kern = sift_attention_kernel<BT, HD, DENSE>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        G::kSmem);
+    });
+    if (attr_err != cudaSuccess) return SIFT_ERR_CUDA;
+    const int sms = device_sm_count();
+    if (sms <= 0) return SIFT_ERR_CUDA;
+    const int grid = p.total_items < sms ? p.total_items : sms;
+    if (grid <= 0) return SIFT_OK;
+    kern<<<grid, kThreads, G::kSmem, stream>>>(mq, mk, mv, p);
+    return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
+}
+
+template <bool DENSE>
+sift_status dispatch(int tile, int hd, const CUtensorMap &mq, const CUtensorMap &mk,
+                     const CUtensorMap &mv, const AttnParams &p, cudaStream_t stream) {
+    if (tile == 128 && hd == 128) return launch_attention<128, 128, DENSE>(mq, mk, mv, p, stream);
+    if (tile == 128 && hd == 64) return launch_attention<128, 64, DENSE>(mq, mk, mv, p, stream);
+    if (tile == 64 && hd == 128) return launch_attention<64, 128, DENSE>(mq, mk, mv, p, stream);
+    if (tile == 64 && hd == 64) return launch_attention<64, 64, DENSE>(mq, mk, mv, p, stream);
+    return SIFT_ERR_UNSUPPORTED;
+}
+
+sift_status prepare(const sift_problem *prob, const void *q, const void *k, const void *v,
+                    float softmax_scale, void *o, float *lse, void *workspace,
+                    size_t workspace_bytes, int32_t *dev_status, CUtensorMap *maps,
+                    AttnParams *p) {
+    sift_status st = validate_problem(prob, true);
+    if (st != SIFT_OK) return st;
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr ||
+        workspace == nullptr || dev_status == nullptr)
+        return SIFT_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0 ||
+        (reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0)
+        return SIFT_ERR_INVALID_ARG;
+    if (workspace_bytes < sift_workspace_bytes(prob)) return SIFT_ERR_INVALID_ARG;
+    const int d = prob->head_dim, B = prob->tile, T = prob->total_tokens;
+    if (!make_map(&maps[0], q, d, prob->num_q_heads, T, B) ||
+        !make_map(&maps[1], k, d, prob->num_kv_heads, T, B) ||
+        !make_map(&maps[2], v, d, prob->num_kv_heads, T, B))
+        return SIFT_ERR_CUDA;
+    const int N = T / B;
+    const int G = prob->num_q_heads / prob->num_kv_heads;
+    AttnParams a{};
+    a.o = static_cast<__nv_bfloat16 *>(o);
+    a.lse = lse;
+    a.work_counter = static_cast<int32_t *>(workspace);
+    a.status = dev_status;
+    a.U = N * prob->num_kv_heads;
+    a.N = N;
+    a.Hq = prob->num_q_heads;
+    a.G = G;
+    a.pairs = G / 2;
+    const int64_t items = static_cast<int64_t>(a.U) * a.pairs;
+    if (items > INT32_MAX / 2) return SIFT_ERR_UNSUPPORTED;
+    a.total_items = static_cast<int32_t>(items);
+    a.rowcap = prob->max_tiles_per_prompt;
+    a.total_tokens = T;
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf(static_cast<float>(d));
+    a.scale_log2 = scale * 1.4426950408889634f;
+    const DebugWaits dw = debug_waits();
+    a.timeout_ns = dw.timeout_ns;
+    a.stall = dw.stall;
+    *p = a;
+    return SIFT_OK;
+}
+
+}  // namespace
+}  // namespace sift
+
+extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t layer, const void *q,
+                                           const void *k, const void *v, const int32_t *kv_idx,
+                                           const int32_t *counts, const int32_t *sched,
+                                           float softmax_scale, void *o, float *lse,
+                                           void *workspace, size_t workspace_bytes,
+                                           int32_t *dev_status, cudaStream_t stream) {
+    using namespace sift;
+    if (prob == nullptr || layer < 0 || layer >= prob->num_layers || kv_idx == nullptr ||
+        counts == nullptr || sched == nullptr)
+        return SIFT_ERR_INVALID_ARG;
+    CUtensorMap maps[3];
+    AttnParams p;
+    sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
+                             dev_status, maps, &p);
+    if (st != SIFT_OK) return st;
+    const int64_t lu = static_cast<int64_t>(layer) * p.U;
+    p.kv_idx = kv_idx + lu * p.rowcap;
+    p.counts = counts + lu;
+    p.sched = sched + lu;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
+    return dispatch<false>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+}
+
+extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const void *k,
+                                          const void *v, float softmax_scale, void *o, float *lse,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *dev_status, cudaStream_t stream) {
+    using namespace sift;
+    CUtensorMap maps[3];
+    AttnParams p;
+    sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
+                             dev_status, maps, &p);
+    if (st != SIFT_OK) return st;
+    int32_t *ws_counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kWsHeader);
+    int32_t *ws_sched = ws_counts + p.U;
+    if (launch_dense_counts(prob, ws_counts, dev_status, stream) != cudaSuccess)
+        return SIFT_ERR_CUDA;
+    if (launch_schedule(ws_counts, ws_sched, 1, p.U, prob->max_tiles_per_prompt, dev_status,
+                        stream) != cudaSuccess)
+        return SIFT_ERR_CUDA;
+    p.kv_idx = nullptr;
+    p.counts = ws_counts;
+    p.sched = ws_sched;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
+    return dispatch<true>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+}

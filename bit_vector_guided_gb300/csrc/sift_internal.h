@@ -1,0 +1,41 @@
+// sift_internal.h -- host-side helpers shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/sift.h"
+
+namespace sift {
+
+// default limit of every device-side wait; the kernels never spin unbounded
+constexpr uint64_t kDefaultWaitTimeoutNs = 2000000000ull;
+
+struct DebugWaits {
+    uint64_t timeout_ns;
+    int32_t stall;
+};
+DebugWaits debug_waits();
+
+// scalar / pointer validation shared by every entry point
+sift_status validate_problem(const sift_problem *p, bool attention);
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// number of SMs of the current device (cached per device)
+int device_sm_count();
+
+// Longest-first ordering of `layers` groups of `units` counts each:
+// sched[l*units + r] = unit with the r-th largest count of group l.
+cudaError_t launch_schedule(const int32_t *counts, int32_t *sched, int layers, int units,
+                            int rowcap, int32_t *dev_status, cudaStream_t stream);
+
+// counts[h*N + i] = number of tiles of prompt(i) up to and including i (dense rows)
+cudaError_t launch_dense_counts(const sift_problem *p, int32_t *counts, int32_t *dev_status,
+                                cudaStream_t stream);
+
+// workspace layout: [0,256) work counter and padding; then dense counts and schedule
+constexpr size_t kWsHeader = 256;
+
+}  // namespace sift

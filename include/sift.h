@@ -1,0 +1,178 @@
+/*
+ * sift.h -- C ABI of the SIFT online-prefill hot path on GB300 (sm_103a).
+ *
+ * SIFT (gist.science/it/paper/2606.09441, "Design del Sistema") keeps, for
+ * every retrieved document, layer and head, two bit vectors: Local-Attention
+ * (LA) bits flag tiles of the document's own causal self-attention matrix,
+ * Cross-Attention (CA) bits flag KV pages (tile columns) of the document that
+ * later documents of the same prompt attend to.  At prefill time a decoding
+ * kernel turns the bits into explicit tile index lists ("Dettagli di
+ * Implementazione", decoding kernel) and a sparse flash-attention kernel
+ * computes only the flagged tiles and skips the rest ("Esecuzione Online";
+ * "Dettagli di Implementazione", sparse attention kernel).  The full
+ * recompute it is measured against ("Risultati") is dense causal attention.
+ *
+ * Readings where the pages are silent (all stated here, applied everywhere):
+ *   - bits are kept per KV head (grouped-query attention shares one list per
+ *     KV head among its query heads);
+ *   - tile size == KV page size == `tile` tokens; every prompt, document and
+ *     suffix boundary is a multiple of `tile`;
+ *   - diagonal tiles are always computed, causally inside the tile;
+ *   - the user-query suffix after the last document attends densely to the
+ *     whole prompt;
+ *   - a CA bit of document g' page j admits that page to every row of every
+ *     later document of the same prompt; LA bits at j >= i are ignored;
+ *   - skipped tiles are excluded from the softmax (exactly -inf);
+ *   - softmax_scale <= 0 means 1/sqrt(head_dim); LSE is a natural log.
+ *
+ * Conventions for every entry point:
+ *   - all array pointers are DEVICE pointers owned by the caller; the library
+ *     allocates no memory and keeps no state between calls;
+ *   - work is enqueued on `stream` and returns without synchronising;
+ *   - arguments are validated on the host before anything is launched
+ *     (SIFT_ERR_INVALID_ARG / SIFT_ERR_UNSUPPORTED, nothing enqueued);
+ *   - a failed launch returns SIFT_ERR_CUDA;
+ *   - problems only visible on the device (inconsistent offsets, an index
+ *     outside its row, a bounded wait that ran out) are written to
+ *     `*dev_status` (device int32, first error wins, never cleared by the
+ *     library: the caller zeroes it and reads it after synchronising).
+ *     Kernels never trap: on such an error they finish or return early, and
+ *     the affected outputs are unspecified.
+ */
+#ifndef SIFT_H
+#define SIFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum {
+    SIFT_OK = 0,
+    SIFT_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, inconsistent sizes          */
+    SIFT_ERR_UNSUPPORTED = 2,   /* valid but not implemented (head_dim, tile, odd GQA)  */
+    SIFT_ERR_CUDA = 3,          /* a CUDA call or launch failed                          */
+    SIFT_ERR_TIMEOUT = 4,       /* device: a bounded wait ran out (written to dev_status) */
+    SIFT_ERR_DEVICE_CHECK = 5   /* device: inconsistent offsets or indices (dev_status)  */
+} sift_status;
+
+/*
+ * One packed varlen batch of prompts.  Prompt p covers tokens
+ * [cu_seqlens[p], cu_seqlens[p+1]); it holds documents doc_cu[p] ..
+ * doc_cu[p+1]-1, laid out back to back from the prompt start (document g ends
+ * at token doc_end[g], exclusive), followed by the user-query suffix up to
+ * the prompt end (possibly empty).  Tiles are numbered globally:
+ * tile i covers tokens [i*tile, (i+1)*tile); N = total_tokens / tile.
+ *
+ * Bit words (uint64, bit j of a row is bit j%64 of word j/64, LSB first):
+ *   LA of document g (T_g tiles, W_g = ceil(T_g/64)) for (layer l, kv head h):
+ *     T_g rows of W_g words at la_words[la_off[g] + (l*Hkv + h)*T_g*W_g + row*W_g];
+ *   CA of document g for (l, h): W_g words at ca_words[ca_off[g] + (l*Hkv + h)*W_g].
+ */
+typedef struct {
+    int32_t num_prompts;           /* P >= 1                                            */
+    int32_t num_docs;              /* D >= 0, all prompts together                      */
+    int32_t num_layers;            /* layers covered by the bit words and by sift_decode */
+    int32_t num_q_heads;           /* Hq                                                */
+    int32_t num_kv_heads;          /* Hkv; Hq/Hkv must be even (query heads go in pairs) */
+    int32_t head_dim;              /* d: 64 or 128                                      */
+    int32_t tile;                  /* tile = page size in tokens: 64 or 128             */
+    int32_t total_tokens;          /* cu_seqlens[P]                                     */
+    int32_t max_tiles_per_prompt;  /* rowcap: capacity of one kv_idx row, >= longest prompt's tiles */
+    int32_t reserved;
+    const int32_t *cu_seqlens;     /* device [P+1]                                      */
+    const int32_t *doc_cu;         /* device [P+1]                                      */
+    const int32_t *doc_end;        /* device [D] (may be NULL when D == 0)              */
+    const int64_t *la_off;         /* device [D]                                        */
+    const int64_t *ca_off;         /* device [D]                                        */
+    int64_t la_words_len;          /* number of uint64 words behind la_words            */
+    int64_t ca_words_len;          /* number of uint64 words behind ca_words            */
+} sift_problem;
+
+/*
+ * Bytes of caller-provided scratch that sift_sparse_prefill and
+ * sift_dense_prefill need for `prob` (a work counter for the persistent
+ * scheduler, plus the dense schedule).  Returns 0 if prob is invalid.
+ */
+size_t sift_workspace_bytes(const sift_problem *prob);
+
+/*
+ * Decode the LA/CA bits of every (layer, kv head, query tile) row into its
+ * list of key tiles to compute, and order each layer's rows longest first
+ * for the persistent attention scheduler.
+ * (SIFT pages, "Dettagli di Implementazione": decoding kernel.)
+ *
+ *   kv_idx  int32 [num_layers][Hkv][N][max_tiles_per_prompt]: row (l,h,i)
+ *           lists counts[l][h][i] global tile indices, strictly ascending:
+ *           CA-flagged pages of the earlier documents of i's prompt, then
+ *           the LA-flagged tiles of i's own document, then i itself; a
+ *           suffix row lists every tile of its prompt up to i.  Entries past
+ *           the count are not written.
+ *   counts  int32 [num_layers][Hkv][N]
+ *   sched   int32 [num_layers][Hkv*N]: a permutation of the units
+ *           u = h*N + i of each layer with non-increasing counts.
+ * Bit-exact for kv_idx and counts.  Two kernel launches.
+ */
+sift_status sift_decode(const sift_problem *prob, const uint64_t *la_words,
+                        const uint64_t *ca_words, int32_t *kv_idx, int32_t *counts,
+                        int32_t *sched, int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Block-sparse causal grouped-query flash attention of one layer over the
+ * decoded lists: each query tile of query head qh attends to the key tiles of
+ * row (layer, qh / (Hq/Hkv), i) only, the diagonal tile causally.
+ * (SIFT pages, "Dettagli di Implementazione": sparse attention kernel.)
+ *
+ *   q       bf16 [total_tokens][Hq][d]   (16-byte aligned, contiguous)
+ *   k, v    bf16 [total_tokens][Hkv][d]
+ *   kv_idx, counts, sched: sift_decode's outputs (all layers; `layer` picks the slice)
+ *   o       bf16 [total_tokens][Hq][d]   output, O = softmax(scale*QK^T) V over the list
+ *   lse     fp32 [Hq][total_tokens]      output, natural-log sum of exp(scale*qk)
+ *   workspace  >= sift_workspace_bytes(prob) bytes of device scratch; clobbered;
+ *              calls that share a workspace must not overlap on the GPU.
+ * One memset and one kernel launch.
+ */
+sift_status sift_sparse_prefill(const sift_problem *prob, int32_t layer, const void *q,
+                                const void *k, const void *v, const int32_t *kv_idx,
+                                const int32_t *counts, const int32_t *sched, float softmax_scale,
+                                void *o, float *lse, void *workspace, size_t workspace_bytes,
+                                int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Dense causal grouped-query flash attention over each whole prompt: the full
+ * recompute baseline of the SIFT pages ("Risultati").  Same kernel as
+ * sift_sparse_prefill with the implicit list {prompt start .. i}; the bit
+ * words, kv_idx and layer are not used.  Same layouts as above.
+ * One memset and three kernel launches (row lengths, schedule, attention).
+ */
+sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const void *k,
+                               const void *v, float softmax_scale, void *o, float *lse,
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               cudaStream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *sift_status_string(sift_status status);
+
+/*
+ * Test hook for the bounded waits (no counterpart on the pages).  Applies to
+ * launches made after the call, process-wide:
+ *   wait_timeout_ns  limit of every device-side wait (0 restores the default,
+ *                    2 s);
+ *   stall_flag       nonzero: the attention kernel's MMA issuer first waits
+ *                    on a barrier that nothing ever signals, so the wait runs
+ *                    out, the kernel unwinds and reports SIFT_ERR_TIMEOUT.
+ */
+void sift_debug_set_waits(uint64_t wait_timeout_ns, int32_t stall_flag);
+
+/* ABI version of this header (major*100 + minor). */
+int32_t sift_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SIFT_H */

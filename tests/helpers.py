@@ -1,0 +1,94 @@
+"""Shared helpers for the GPU parity tests (inputs from `workloads`, reference from `oracle`)."""
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+
+# spec tolerances for attention outputs on N(0,1) inputs against the oracle
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+LSE_REL = 1e-3
+
+
+def device_bits(la, ca, device="cuda"):
+    """uint64 words -> int64 device tensors holding the same bytes."""
+    def up(a):
+        a = np.ascontiguousarray(a, np.uint64)
+        if a.size == 0:
+            a = np.zeros(1, np.uint64)
+        return torch.from_numpy(a.view(np.int64)).to(device)
+    return up(la), up(ca)
+
+
+def setup(cfg, device="cuda"):
+    import bit_vector_guided_gb300 as sift
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, device)
+    la_d, ca_d = device_bits(la, ca, device)
+    return lay, la, ca, prob, la_d, ca_d
+
+
+def check_sched(sched, counts):
+    """Each layer's schedule is a permutation of its units with non-increasing counts."""
+    L = counts.shape[0]
+    flat = counts.reshape(L, -1)
+    for l in range(L):
+        s = sched[l]
+        assert np.array_equal(np.sort(s), np.arange(flat.shape[1])), "sched is not a permutation"
+        c = flat[l][s]
+        assert np.all(np.diff(c) <= 0), "sched is not longest-first"
+
+
+def attention_errors(o_gpu, lse_gpu, o_ref, lse_ref):
+    """Errors of GPU rows against oracle rows (same shapes, any leading layout)."""
+    o = np.asarray(o_gpu, np.float64)
+    e = np.abs(o - o_ref)
+    lrel = np.abs(np.asarray(lse_gpu, np.float64) - lse_ref) / np.maximum(np.abs(lse_ref), 1e-30)
+    return float(e.max()), float(e.mean()), float(lrel.max())
+
+
+def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    mx, mean, lrel = attention_errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    assert np.isfinite(np.asarray(o_gpu, np.float64)).all(), f"{what}: non-finite output"
+    assert mx <= MAX_ABS, f"{what}: max abs {mx:.3g} > {MAX_ABS}"
+    assert mean <= MEAN_ABS, f"{what}: mean abs {mean:.3g} > {MEAN_ABS}"
+    assert lrel <= LSE_REL, f"{what}: lse rel {lrel:.3g} > {LSE_REL}"
+    return mx, mean, lrel
+
+
+def sample_pairs(lay, rng, n_random=24):
+    """(query tile, query head) pairs to check on a large batch: the first tile of each
+    prompt, the last document tile and the last suffix tile of each prompt, plus random
+    ones."""
+    B = lay.tile
+    Hq = lay.num_q_heads
+    pairs = set()
+    for p in range(lay.num_prompts):
+        t0 = int(lay.cu_seqlens[p]) // B
+        t1 = int(lay.cu_seqlens[p + 1]) // B
+        docs = range(lay.doc_cu[p], lay.doc_cu[p + 1])
+        last_doc_tile = (int(lay.doc_end[docs[-1]]) // B - 1) if len(docs) else t0
+        for t in (t0, last_doc_tile, t1 - 1):
+            pairs.add((t, int(rng.integers(Hq))))
+    N = lay.num_tiles
+    for _ in range(n_random):
+        pairs.add((int(rng.integers(N)), int(rng.integers(Hq))))
+    return sorted(pairs)
+
+
+def oracle_rows_for_pairs(lay, la, ca, layer, q, k, v, pairs):
+    B = lay.tile
+    tok = np.concatenate([np.arange(i * B, (i + 1) * B) for i, _ in pairs]).astype(np.int32)
+    head = np.concatenate([np.full(B, h) for _, h in pairs]).astype(np.int32)
+    o, lse = oracle.attention_rows(lay, la, ca, layer, q, k, v, tok, head)
+    return tok, head, o, lse
+
+
+def gpu_rows(o_gpu, lse_gpu, tok, head):
+    o = o_gpu[torch.as_tensor(tok, device=o_gpu.device).long(),
+              torch.as_tensor(head, device=o_gpu.device).long()].double().cpu().numpy()
+    lse = lse_gpu[torch.as_tensor(head, device=o_gpu.device).long(),
+                  torch.as_tensor(tok, device=o_gpu.device).long()].double().cpu().numpy()
+    return o, lse
