@@ -1,0 +1,548 @@
+"""Benchmark of the SIFT online-prefill hot path on GB300.
+
+One step = the whole hot path over one batch: ``sift_decode`` of the bit
+vectors of every layer (one decode + one schedule launch), then
+``sift_sparse_prefill`` for every layer (fresh seeded Q/K/V per layer, resident
+in HBM).  Default workload: Llama-3.1-8B heads (32 q / 8 kv, d = 128), one
+prompt of 16 docs x 2048 tokens + 256-token query (33,024 tokens), 32 layers,
+per-(layer, kv head) LA density U[0.05, 0.35] and CA half of it, tile 128.
+
+Metric: sparse-prefill attention TFLOP/s counting every computed tile at
+4*B^2*d per query head (diagonal tiles in full), plus ms per layer against the
+dense causal kernel on the same GPU.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same per-GPU workload (replicas,
+weak scaling, no collective on the data path); timing is the max over ranks.
+``--impl reference`` times the CPU oracle (the only reference this method has)
+on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "sparse-prefill attention TFLOP/s (computed tiles) & % bf16 peak; ms per layer vs dense"
+UNIT = "TFLOP/s"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sift_sparse_prefill_llama_32k.md")
+
+
+def tile_flops(cfg) -> float:
+    """FLOPs of one computed tile for one query head: QK^T and PV, 2*B*B*d each."""
+    return 4.0 * cfg.tile * cfg.tile * cfg.head_dim
+
+
+def computed_flops(cfg, counts: np.ndarray) -> np.ndarray:
+    """Per-layer FLOPs over computed tiles: sum of row counts x query heads per kv head."""
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    return counts.reshape(counts.shape[0], -1).sum(axis=1).astype(np.float64) * G * tile_flops(cfg)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_vector_guided_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("sift_attention") or name == "ptx.cuh":
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the sparse kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    vals = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, _, v = line.strip()[2:].partition(":")
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256_16") != kernel_source_digest():
+        return None
+    try:
+        return float(vals["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(cfg, lay, la, ca, q, k, v, counts, budget_s: float, seed: int = 7):
+    """Time the oracle on (query tile, query head) pairs of layer 0 until ~budget_s of CPU
+    work; returns (flops counted as computed tiles, seconds, threads, pairs)."""
+    import oracle
+    threads = oracle.set_threads(0)
+    rng = np.random.default_rng(seed)
+    B, G = cfg.tile, cfg.num_q_heads // cfg.num_kv_heads
+    N = lay.num_tiles
+    flops = secs = 0.0
+    pairs = 0
+    batch = 1
+    while secs < budget_s and pairs < 4096:
+        sel = [(int(rng.integers(N)), int(rng.integers(cfg.num_q_heads))) for _ in range(batch)]
+        tok = np.concatenate([np.arange(i * B, (i + 1) * B) for i, _ in sel]).astype(np.int32)
+        head = np.concatenate([np.full(B, h) for _, h in sel]).astype(np.int32)
+        t0 = time.perf_counter()
+        oracle.attention_rows(lay, la, ca, 0, q, k, v, tok, head)
+        secs += time.perf_counter() - t0
+        flops += sum(float(counts[0, h // G, i]) for i, h in sel) * tile_flops(cfg)
+        pairs += batch
+        batch = min(batch * 2, 64)
+    return flops, secs, threads, pairs
+
+
+def host_inputs_layer0(cfg):
+    import torch
+    return W.make_qkv(cfg, 0, device="cpu")
+
+
+def run_reference(args, cfg):
+    """--impl reference: the CPU oracle on a bounded sample of the same workload."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    oracle.build()
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    _, counts = oracle.decode(lay, la, ca)
+    q, k, v = host_inputs_layer0(cfg)
+    per_step = max(1.0, min(10.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(cfg, lay, la, ca, q, k, v, counts, per_step / 4, seed=1)
+    tot_f = tot_s = 0.0
+    tot_pairs = 0
+    threads = 1
+    for s in range(args.steps):
+        f, sec, threads, pairs = oracle_sample(cfg, lay, la, ca, q, k, v, counts, per_step,
+                                               seed=100 + s)
+        tot_f += f
+        tot_s += sec
+        tot_pairs += pairs
+    value = tot_f / tot_s / 1e12
+    out = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(cfg, args, lay),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{tot_pairs} random (query tile, query head) pairs of "
+                                   f"layer 0 ({cfg.tile} rows each), ~{per_step:.0f} s per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+    return 0
+
+
+def config_dict(cfg, args, lay):
+    return {"workload": cfg.name, "description": cfg.description, "tokens": lay.total_tokens,
+            "layers": cfg.num_layers, "q_heads": cfg.num_q_heads, "kv_heads": cfg.num_kv_heads,
+            "head_dim": cfg.head_dim, "tile": cfg.tile, "prompts": lay.num_prompts,
+            "docs": lay.num_docs,
+            "l2": "inputs larger than L2: each layer's Q/K/V/O (> 129 MB) is distinct and "
+                  "the step cycles through every layer",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+def run_ours(args, cfg):
+    import torch
+    import bit_vector_guided_gb300 as sift
+    from bit_vector_guided_gb300 import build as sbuild
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    if rank == 0:
+        sbuild.build()
+    if dist is not None:
+        dist.barrier()
+    sift.load_library()
+
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, dev)
+    la_d = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).to(dev)
+    ca_d = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).to(dev)
+    L = cfg.num_layers
+    qkv = [W.make_qkv(cfg, l, device=dev) for l in range(L)]
+    outs = [(torch.empty_like(q), torch.empty((cfg.num_q_heads, lay.total_tokens),
+                                              dtype=torch.float32, device=dev))
+            for q, _, _ in qkv]
+    H, N, R = cfg.num_kv_heads, lay.num_tiles, lay.max_tiles_per_prompt
+    kv_idx = torch.empty((L, H, N, R), dtype=torch.int32, device=dev)
+    counts = torch.empty((L, H, N), dtype=torch.int32, device=dev)
+    sched = torch.empty((L, H * N), dtype=torch.int32, device=dev)
+    status = prob.new_status()
+    ws = prob.new_workspace()
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        if events is not None:
+            events[0].record(stream)
+        sift.decode(prob, la_d, ca_d, kv_idx, counts, sched, dev_status=status, stream=stream)
+        if events is not None:
+            events[1].record(stream)
+        for l in range(L):
+            q, k, v = qkv[l]
+            o, lse = outs[l]
+            sift.sparse_prefill(prob, l, q, k, v, kv_idx, counts, sched, 0.0, o, lse, ws,
+                                status, stream)
+            if events is not None:
+                events[2 + l].record(stream)
+
+    # warm-up (also fills counts for the FLOP count)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + sift.status_string(int(status.item())))
+    counts_h = counts.cpu().numpy()
+    flops_layer = computed_flops(cfg, counts_h)
+    flops_step = float(flops_layer.sum())
+
+    # timed region: K steps, events per launch on the launching stream
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 2)] for _ in range(args.steps)]
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + sift.status_string(int(status.item())))
+    decode_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
+    layer_ms = np.array([[ev[s][1 + l].elapsed_time(ev[s][2 + l]) for l in range(L)]
+                         for s in range(args.steps)])
+    ms_per_step = total_ms / args.steps
+    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    kern_ms = float(layer_ms.mean())
+    achieved = float(flops_layer.mean()) / (kern_ms * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    traffic = profiled_traffic()
+
+    # dense baseline on the same GPU (a few layers), outside the timed region
+    dense_layers = list(range(min(L, 4)))
+    dense_ms = []
+    for rep in range(3):
+        for l in dense_layers:
+            q, k, v = qkv[l]
+            o, lse = outs[l]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            sift.dense_prefill(prob, q, k, v, 0.0, o, lse, ws, status, stream)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            if rep > 0:
+                dense_ms.append(e0.elapsed_time(e1))
+    dense_ms_layer = float(np.mean(dense_ms))
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    dense_flops_layer = float(sum(
+        (n * (n + 1) // 2) for n in np.diff(lay.cu_seqlens) // cfg.tile)) * H * G * tile_flops(cfg)
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": config_dict(cfg, args, lay),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "sift_sparse_prefill",
+                     "peak_source": f"bf16_tflops_sustained of {peak_src}"},
+        "gpu_launches": args.steps * (2 + L),
+        "sparse_ms_per_layer": kern_ms,
+        "sparse_ms_per_layer_p90": float(np.percentile(layer_ms.mean(axis=0), 90)),
+        "dense_ms_per_layer": dense_ms_layer,
+        "dense_tflops": dense_flops_layer / (dense_ms_layer * 1e-3) / 1e12,
+        "speedup_vs_dense": dense_ms_layer / kern_ms,
+        "computed_tile_fraction": float(flops_layer.mean() / dense_flops_layer),
+        "decode_us": 1e3 * float(np.median(decode_ms)),
+        "decode_launches_per_step": 2,
+    }
+    clocks = clk.summary()
+    result["clocks"] = clocks
+
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched,
+                                status, ws, stream, dev, flops_step, world, dist)
+    if not args.no_sweep and rank == 0 and world == 1:
+        result["density_sweep"] = run_sweep(args, dev, stream)
+    del qkv, outs
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        q0, k0, v0 = host_inputs_layer0(cfg)
+        _, counts_o = oracle.decode(lay, la, ca)
+        f, sec, thr, pairs = oracle_sample(cfg, lay, la, ca, q0, k0, v0, counts_o,
+                                           args.cpu_seconds)
+        result["cpu_baseline"] = {
+            "value": f / sec / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{pairs} random (query tile, query head) pairs of layer 0, "
+                      f"{cfg.tile} query rows each, {sec:.1f} s on {thr} threads"}
+    if dist is not None:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+    return 0
+
+
+def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, status, ws, stream,
+            dev, flops_step, world, dist):
+    """Same metric through the public API with host buffers: every step copies that step's
+    inputs (bits of all layers + Q/K/V of every layer) from pinned host memory and reads
+    every layer's O and LSE back to pinned host memory."""
+    import torch
+    import bit_vector_guided_gb300 as sift
+    L = cfg.num_layers
+    la_h = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).pin_memory()
+    ca_h = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).pin_memory()
+    la_d = torch.empty_like(la_h, device=dev)
+    ca_d = torch.empty_like(ca_h, device=dev)
+    host_in = [tuple(t.cpu().pin_memory() for t in qkv[l]) for l in range(L)]
+    host_out = [(torch.empty(o.shape, dtype=o.dtype).pin_memory(),
+                 torch.empty(lse.shape, dtype=lse.dtype).pin_memory()) for o, lse in outs]
+    h2d = (la_h.numel() + ca_h.numel()) * 8 + sum(t.numel() * t.element_size()
+                                                  for tri in host_in for t in tri)
+    d2h = sum(o.numel() * o.element_size() + s.numel() * s.element_size() for o, s in host_out)
+    copy = torch.cuda.Stream(dev)
+    done_in = [torch.cuda.Event() for _ in range(L)]
+    done_kern = [torch.cuda.Event() for _ in range(L)]
+
+    def step():
+        # copies on a side stream overlap with the kernels of earlier layers; a step's
+        # uploads wait for the previous step's kernels (they overwrite the same buffers)
+        copy.wait_stream(stream)
+        with torch.cuda.stream(copy):
+            la_d.copy_(la_h, non_blocking=True)
+            ca_d.copy_(ca_h, non_blocking=True)
+        ev_bits = torch.cuda.Event()
+        ev_bits.record(copy)
+        for l in range(L):
+            with torch.cuda.stream(copy):
+                for dst, src in zip(qkv[l], host_in[l]):
+                    dst.copy_(src, non_blocking=True)
+                done_in[l].record(copy)
+        stream.wait_event(ev_bits)
+        sift.decode(prob, la_d, ca_d, kv_idx, counts, sched, dev_status=status, stream=stream)
+        for l in range(L):
+            stream.wait_event(done_in[l])
+            q, k, v = qkv[l]
+            o, lse = outs[l]
+            sift.sparse_prefill(prob, l, q, k, v, kv_idx, counts, sched, 0.0, o, lse, ws,
+                                status, stream)
+            done_kern[l].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(done_kern[l])
+                host_out[l][0].copy_(o, non_blocking=True)
+                host_out[l][1].copy_(lse, non_blocking=True)
+        stream.wait_stream(copy)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, min(args.steps, 5))
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(dev)
+    el = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([el], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    return {"value": world * flops_step * steps / el / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": 1e3 * el / steps, "steps": steps,
+            "note": "pinned host buffers; H2D of each layer's Q/K/V and D2H of its O/LSE on a "
+                    "copy stream overlapping the kernels"}
+
+
+def run_sweep(args, dev, stream):
+    """Sparse vs dense at each LA=CA density of the batch-of-4 configuration."""
+    import torch
+    import bit_vector_guided_gb300 as sift
+    rows = []
+    base = W.get_config("batch4_p100")
+    q, k, v = W.make_qkv(base, 0, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((base.num_q_heads, base.total_tokens), dtype=torch.float32, device=dev)
+    dense_ms = None
+    for name in ("batch4_p005", "batch4_p010", "batch4_p020", "batch4_p040", "batch4_p070",
+                 "batch4_p100"):
+        cfg = W.get_config(name)
+        lay = W.make_layout(cfg)
+        la, ca = W.make_bits(cfg, lay)
+        prob = sift.SiftProblem.from_layout(lay, dev)
+        la_d = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).to(dev)
+        ca_d = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).to(dev)
+        st = prob.new_status()
+        ws = prob.new_workspace()
+        kv, cnt, sch = sift.decode(prob, la_d, ca_d, dev_status=st, stream=stream)
+
+        def timed(fn, reps=5):
+            for _ in range(2):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            return e0.elapsed_time(e1) / reps
+
+        sp = timed(lambda: sift.sparse_prefill(prob, 0, q, k, v, kv, cnt, sch, 0.0, o, lse, ws,
+                                               st, stream))
+        if dense_ms is None:
+            dense_ms = timed(lambda: sift.dense_prefill(prob, q, k, v, 0.0, o, lse, ws, st,
+                                                        stream))
+        fl = float(computed_flops(cfg, cnt.cpu().numpy())[0])
+        rows.append({"workload": name, "density": cfg.bits.la_p, "sparse_ms": sp,
+                     "dense_ms": dense_ms, "speedup": dense_ms / sp,
+                     "sparse_tflops": fl / (sp * 1e-3) / 1e12})
+        if int(st.item()) != 0:
+            raise RuntimeError("sweep device status " + sift.status_string(int(st.item())))
+    return rows
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama_32k", choices=sorted(W.CONFIGS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling only: keep the first N layers of the workload (the JSON "
+                         "line then names the reduced workload)")
+    args = ap.parse_args(argv)
+    if args.warmup < 1:
+        ap.error("--warmup must be >= 1 (timed runs use >= 3)")
+    cfg = W.get_config(args.config)
+    if args.layers and args.layers < cfg.num_layers:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, num_layers=args.layers,
+                                  name=f"{cfg.name}", description=cfg.description +
+                                  f" [first {args.layers} layers only]")
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,101 @@
+"""Full-size workloads in the launch configuration bench.py times (decode of all
+layers, then one sparse launch per layer on the same stream), checked on
+sampled (query tile, query head) pairs against the oracle and, over every row,
+against properties that hold at any size.
+
+SIFT pages (gist.science/it/paper/2606.09441), "Risultati": Llama-3.1-8B and
+Qwen3-235B-A22B at 32K-64K contexts; the configurations below are synthetic
+stand-ins with those head layouts and lengths.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import (assert_attention_close, gpu_rows, oracle_rows_for_pairs, sample_pairs,
+                     setup)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sift(cuda_device):
+    from bit_vector_guided_gb300 import build
+    build.build()
+    import bit_vector_guided_gb300 as s
+    s.load_library()
+    return s
+
+
+def _convex_bound_ok(o, v, G):
+    """Each output row is a convex combination of V rows: |O| <= max |V| per channel."""
+    vmax = v.float().abs().amax(dim=0).repeat_interleave(G, dim=0)  # [Hq, d]
+    return bool((o.float().abs() <= vmax[None] * (1 + 2 ** -7) + 1e-6).all().item())
+
+
+def _check_layer(sift, cfg, lay, la, ca, layer, q, k, v, o, lse, rng):
+    assert torch.isfinite(o.float()).all().item() and torch.isfinite(lse).all().item()
+    assert _convex_bound_ok(o, v, cfg.num_q_heads // cfg.num_kv_heads)
+    pairs = sample_pairs(lay, rng)
+    qh, kh, vh = q.cpu(), k.cpu(), v.cpu()
+    tok, head, O, LSE = oracle_rows_for_pairs(lay, la, ca, layer, qh, kh, vh, pairs)
+    og, lg = gpu_rows(o, lse, tok, head)
+    return assert_attention_close(og, lg, O, LSE, f"{cfg.name} layer {layer}")
+
+
+@pytest.mark.parametrize("name", ["llama_10doc", "qwen3_64k", "batch4_p005", "batch4_p020",
+                                  "batch4_p040"])
+def test_single_layer_configs(sift, name):
+    cfg = W.get_config(name)
+    lay, la, ca, prob, la_d, ca_d = setup(cfg)
+    st = prob.new_status()
+    ws = prob.new_workspace()
+    stream = torch.cuda.current_stream()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st, stream=stream)
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    o, lse = sift.sparse_prefill(prob, 0, q, k, v, kv, cnt, sched, 0.0, None, None, ws, st,
+                                 stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, sift.status_string(int(st.item()))
+    _check_layer(sift, cfg, lay, la, ca, 0, q, k, v, o, lse, np.random.default_rng(3))
+
+
+def test_llama_32k_all_layers(sift):
+    """Config of the benchmark: 32 layers, one decode launch for all of them."""
+    cfg = W.get_config("llama_32k")
+    lay, la, ca, prob, la_d, ca_d = setup(cfg)
+    st = prob.new_status()
+    ws = prob.new_workspace()
+    stream = torch.cuda.current_stream()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st, stream=stream)
+    kv_o, cnt_o = oracle.decode(lay, la, ca)
+    assert np.array_equal(cnt.cpu().numpy(), cnt_o)
+    rng = np.random.default_rng(11)
+    for layer in range(cfg.num_layers):
+        q, k, v = W.make_qkv(cfg, layer, device="cuda")
+        o, lse = sift.sparse_prefill(prob, layer, q, k, v, kv, cnt, sched, 0.0, None, None, ws,
+                                     st, stream)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, sift.status_string(int(st.item()))
+        if layer in (0, 13, 31):
+            _check_layer(sift, cfg, lay, la, ca, layer, q, k, v, o, lse, rng)
+        else:
+            assert torch.isfinite(o.float()).all().item()
+            assert _convex_bound_ok(o, v, cfg.num_q_heads // cfg.num_kv_heads)
+
+
+def test_batch4_full_density_equals_dense(sift):
+    """At 100% density the sparse kernel computes what the dense kernel computes."""
+    cfg = W.get_config("batch4_p100")
+    lay, la, ca, prob, la_d, ca_d = setup(cfg)
+    st = prob.new_status()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st)
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    o, lse = sift.sparse_prefill(prob, 0, q, k, v, kv, cnt, sched, dev_status=st)
+    od, lsed = sift.dense_prefill(prob, q, k, v, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert (o.float() - od.float()).abs().max().item() <= 1e-2
+    assert (lse - lsed).abs().max().item() <= 1e-4
+    _check_layer(sift, cfg, lay, la, ca, 0, q, k, v, od, lsed, np.random.default_rng(5))
