@@ -27,7 +27,8 @@
  *
  * Conventions for every entry point:
  *   - all array pointers are DEVICE pointers owned by the caller; the library
- *     allocates no memory and keeps no state between calls;
+ *     allocates no memory and keeps no state between calls (except the fixed
+ *     scratch array of sift_dense_prefill_noalloc, described there);
  *   - work is enqueued on `stream` and returns without synchronising;
  *   - arguments are validated on the host before anything is launched
  *     (SIFT_ERR_INVALID_ARG / SIFT_ERR_UNSUPPORTED, nothing enqueued);
@@ -153,6 +154,30 @@ sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const vo
                                const void *v, float softmax_scale, void *o, float *lse,
                                void *workspace, size_t workspace_bytes, int32_t *dev_status,
                                cudaStream_t stream);
+
+/*
+ * sift_dense_prefill for callers that cannot allocate device memory at call
+ * time (the SIFT pages have no counterpart; this is a deployment aid).  A
+ * serving runtime that plans all of its buffers at start-up, code that must
+ * not risk the implicit device synchronisation of cudaMalloc/cudaFree, or a
+ * host thread without an allocator can call this instead: it takes no
+ * workspace and uses a scratch array that the library keeps in device memory.
+ *   - Same arguments, layouts and results as sift_dense_prefill, minus the
+ *     workspace.
+ *   - The scratch is a fixed 1 MiB array per GPU, held from the moment the
+ *     library is loaded on that GPU until the process exits.  A problem whose
+ *     sift_workspace_bytes() exceeds 1 MiB (about 131,000 kv-head x query-tile
+ *     units) is rejected with SIFT_ERR_UNSUPPORTED before anything is enqueued.
+ *   - The first call on a device looks up the array's device address, with
+ *     that device current; make that first call outside any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents:
+ *     calls whose work may overlap on the GPU (different streams, or several
+ *     host threads) race on it and must be serialised by the caller.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ */
+sift_status sift_dense_prefill_noalloc(const sift_problem *prob, const void *q, const void *k,
+                                       const void *v, float softmax_scale, void *o, float *lse,
+                                       int32_t *dev_status, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *sift_status_string(sift_status status);
