@@ -13,7 +13,8 @@
 // decoded list of row (h, i).  Roles inside the 320-thread CTA:
 //   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax of head slot 1
-//   warp  8    scheduler + TMA producer (Q pair, then K_j, V_j into a 4-stage ring)
+//   warp  8    scheduler + TMA producer (Q pair, then K_j into a 3-slot ring and V_j into
+//              a 2-slot ring; K is consumed first, so it gets the deeper prefetch)
 //   warp  9    TMEM allocator + single-thread MMA issuer
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
@@ -41,7 +42,8 @@ namespace {
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 4;
+constexpr int kKSlots = 3;  // K ring: K_j is consumed first, so it gets the deeper ring
+constexpr int kVSlots = 2;  // V ring
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all of TMEM)
@@ -58,7 +60,7 @@ struct WorkItem {
 
 struct Ctl {
     uint64_t q_full, q_empty;
-    uint64_t kv_full[kStages], kv_empty[kStages];
+    uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots], v_empty[kVSlots];
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t sch_full[2], sch_empty[2];
     uint64_t teardown, never;
@@ -88,8 +90,9 @@ struct Geo {
     static constexpr int kQBytes = 2 * kBoxes * kQBox;
     static constexpr int kKVBox = BT * 128;
     static constexpr int kKVBytes = kBoxes * kKVBox;
-    static constexpr int kRingOff = kQBytes;
-    static constexpr int kCtlOff = kQBytes + kStages * kKVBytes;
+    static constexpr int kKOff = kQBytes;
+    static constexpr int kVOff = kKOff + kKSlots * kKVBytes;
+    static constexpr int kCtlOff = kVOff + kVSlots * kKVBytes;
     static constexpr int kSmemUsed = kCtlOff + 1024 + 1024;  // + control block + align slack
     static constexpr int kSmem = kSmemUsed > kMinSmem ? kSmemUsed : kMinSmem;
     static constexpr uint32_t kTxQ = 2 * kBoxes * BT * 128;
@@ -127,11 +130,16 @@ __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, uint64_t t
     return true;
 }
 
+// bounded wait with an inlined fast path for a phase that has already completed (a
+// call into the slow path costs hundreds of cycles on the MMA issuer's critical path)
+__device__ __forceinline__ bool wait1(Ctl &c, uint32_t bar, uint32_t parity, const AttnParams &p) {
+    return ptx::mbar_try_wait(bar, parity) || wait_bar(c, bar, parity, p.timeout_ns, p.status);
+}
+
 // all lanes wait, result made warp-uniform
 __device__ __forceinline__ bool wait_warp(Ctl &c, uint32_t bar, uint32_t parity,
                                           const AttnParams &p) {
-    const bool ok = wait_bar(c, bar, parity, p.timeout_ns, p.status);
-    return __all_sync(kFull, ok);
+    return __all_sync(kFull, wait1(c, bar, parity, p));
 }
 
 template <bool DENSE>
@@ -173,7 +181,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     uint8_t *smem = smem_raw + pad;
     const uint32_t sbase = raw + pad;
     const uint32_t q_s = sbase;
-    const uint32_t ring_s = sbase + G::kRingOff;
+    const uint32_t k_s = sbase + G::kKOff;
+    const uint32_t v_s = sbase + G::kVOff;
     Ctl &c = *reinterpret_cast<Ctl *>(smem + G::kCtlOff);
 
     const int warp = threadIdx.x >> 5;
@@ -184,9 +193,13 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     if (threadIdx.x == 0) {
         ptx::mbar_init(B_(c.q_full), 1);
         ptx::mbar_init(B_(c.q_empty), 1);
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(B_(c.kv_full[s]), 1);
-            ptx::mbar_init(B_(c.kv_empty[s]), 1);
+        for (int s = 0; s < kKSlots; ++s) {
+            ptx::mbar_init(B_(c.k_full[s]), 1);
+            ptx::mbar_init(B_(c.k_empty[s]), 1);
+        }
+        for (int s = 0; s < kVSlots; ++s) {
+            ptx::mbar_init(B_(c.v_full[s]), 1);
+            ptx::mbar_init(B_(c.v_empty[s]), 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(B_(c.s_full[s]), 1);
@@ -216,8 +229,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------ scheduler + TMA producer
-        int item_k = 0, qk = 0, f = 0;
+        int item_k = 0, qk = 0, kf = 0, vf = 0;
         bool alive = true;
+        const uint64_t pol_kv = ptx::policy_evict_last();   // K/V tiles are re-read by many items
+        const uint64_t pol_q = ptx::policy_evict_first();   // Q is read once per item
         while (alive) {
             int w = 0;
             if (lane == 0) w = atomicAdd(p.work_counter, 1);
@@ -237,8 +252,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 ptx::mbar_arrive_expect_tx(B_(c.q_full), G::kTxQ);
                 for (int s = 0; s < 2; ++s)
                     for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_load_3d(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ, B_(c.q_full),
-                                         64 * b, it.hq0 + s, it.i * BT);
+                        ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
+                                              B_(c.q_full), 64 * b, it.hq0 + s, it.i * BT, pol_q);
             }
             ++qk;
             for (int jb = 0; jb < it.n && alive; jb += 32) {
@@ -259,30 +274,42 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const int cnt = min(32, it.n - jb);
                 for (int jj = 0; jj < cnt; ++jj) {
                     const int idx = __shfl_sync(kFull, my, jj);
-                    for (int kind = 0; kind < 2; ++kind) {
-                        const int slot2 = f % kStages;
-                        if (!wait_warp(c, B_(c.kv_empty[slot2]), ((f / kStages) & 1) ^ 1, p)) {
-                            alive = false;
-                            break;
-                        }
-                        if (lane == 0) {
-                            ptx::mbar_arrive_expect_tx(B_(c.kv_full[slot2]), G::kTxKV);
-                            const uint32_t dst = ring_s + slot2 * G::kKVBytes;
-                            for (int b = 0; b < G::kBoxes; ++b)
-                                ptx::tma_load_3d(dst + b * G::kKVBox, kind ? &tmV : &tmK,
-                                                 B_(c.kv_full[slot2]), 64 * b, it.h, idx * BT);
-                        }
-                        ++f;
+                    const int ks = kf % kKSlots;
+                    if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) {
+                        alive = false;
+                        break;
                     }
-                    if (!alive) break;
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
+                        for (int b = 0; b < G::kBoxes; ++b)
+                            ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox, &tmK,
+                                                  B_(c.k_full[ks]), 64 * b, it.h, idx * BT, pol_kv);
+                    }
+                    ++kf;
+                    const int vs = vf % kVSlots;
+                    if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) {
+                        alive = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
+                        for (int b = 0; b < G::kBoxes; ++b)
+                            ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox, &tmV,
+                                                  B_(c.v_full[vs]), 64 * b, it.h, idx * BT, pol_kv);
+                    }
+                    ++vf;
                 }
             }
         }
         if (c.abort && lane == 0) {
             // unwinding: let every copy already issued land before shared memory is released
-            for (int s = 0; s < kStages && s < f; ++s) {
-                const int last = s + ((f - 1 - s) / kStages) * kStages;  // last fill of slot s
-                drain_bar(B_(c.kv_full[s]), (last / kStages) & 1, p.timeout_ns);
+            for (int s = 0; s < kKSlots && s < kf; ++s) {
+                const int last = s + ((kf - 1 - s) / kKSlots) * kKSlots;  // last fill of slot s
+                drain_bar(B_(c.k_full[s]), (last / kKSlots) & 1, p.timeout_ns);
+            }
+            for (int s = 0; s < kVSlots && s < vf; ++s) {
+                const int last = s + ((vf - 1 - s) / kVSlots) * kVSlots;
+                drain_bar(B_(c.v_full[s]), (last / kVSlots) & 1, p.timeout_ns);
             }
             if (qk > 0) drain_bar(B_(c.q_full), (qk - 1) & 1, p.timeout_ns);
         }
@@ -291,12 +318,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         // ------------------------------------------------ single-thread MMA issuer
         if (lane == 0) {
             if (p.stall) wait_bar(c, B_(c.never), 0, p.timeout_ns, p.status);
-            int item_k = 0, qk = 0, f = 0;
+            int item_k = 0, qk = 0, t = 0;  // t: key tiles consumed, same order as the producer
             uint32_t pph0 = 0, pph1 = 0;
             const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-            auto issue_s = [&](int s, int slot) {
+            auto issue_s = [&](int s, int ks) {
                 const uint32_t qa = q_s + s * G::kBoxes * G::kQBox;
-                const uint32_t kb = ring_s + slot * G::kKVBytes;
+                const uint32_t kb = k_s + ks * G::kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off_q = (kk >> 2) * G::kQBox + (kk & 3) * 32;
@@ -305,8 +332,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                                  ptx::sdesc_sw128(kb + off_k, 16, 1024), G::kIdescS, kk > 0);
                 }
             };
-            auto issue_pv = [&](int s, int slot, bool acc) {
-                const uint32_t vb = ring_s + slot * G::kKVBytes;
+            auto issue_pv = [&](int s, int vs, bool acc) {
+                const uint32_t vb = v_s + vs * G::kKVBytes;
 #pragma unroll
                 for (int kk = 0; kk < BT / 16; ++kk) {
                     ptx::umma_ts(s ? tO1 : tO0, (s ? tS1 : tS0) + kk * 8,
@@ -316,66 +343,59 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             };
             while (!c.abort) {
                 const int slot = item_k & 1;
-                if (!wait_bar(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p.timeout_ns, p.status))
-                    break;
+                if (!wait1(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
                 const WorkItem it = c.items[slot];
                 ptx::mbar_arrive(B_(c.sch_empty[slot]));
                 ++item_k;
                 if (!it.valid) break;
-                if (!wait_bar(c, B_(c.q_full), qk & 1, p.timeout_ns, p.status)) break;
+                if (!wait1(c, B_(c.q_full), qk & 1, p)) break;
                 ++qk;
                 ptx::tc_fence_after();
                 bool ok = true;
-                int fVp = 0;
-                for (int j = 0; j < it.n; ++j) {
-                    const int fK = f, fV = f + 1;
-                    f += 2;
-                    if (!wait_bar(c, B_(c.kv_full[fK % kStages]), (fK / kStages) & 1,
-                                  p.timeout_ns, p.status)) { ok = false; break; }
+                for (int j = 0; j < it.n; ++j, ++t) {
+                    const int ks = t % kKSlots;
+                    if (!wait1(c, B_(c.k_full[ks]), (t / kKSlots) & 1, p)) { ok = false; break; }
                     ptx::tc_fence_after();
+                    const int vp = (t + kVSlots - 1) % kVSlots;  // slot of V_{j-1}
                     if (j > 0) {
-                        if (!wait_bar(c, B_(c.kv_full[fVp % kStages]), (fVp / kStages) & 1,
-                                      p.timeout_ns, p.status)) { ok = false; break; }
-                        if (!wait_bar(c, B_(c.p_full[0]), pph0, p.timeout_ns, p.status)) {
+                        if (!wait1(c, B_(c.v_full[vp]), ((t - 1) / kVSlots) & 1, p) ||
+                            !wait1(c, B_(c.p_full[0]), pph0, p)) {
                             ok = false;
                             break;
                         }
                         pph0 ^= 1;
                         ptx::tc_fence_after();
-                        issue_pv(0, fVp % kStages, j > 1);
+                        issue_pv(0, vp, j > 1);
                     }
-                    issue_s(0, fK % kStages);
+                    issue_s(0, ks);
                     ptx::umma_commit(B_(c.s_full[0]));
                     if (j > 0) {
-                        if (!wait_bar(c, B_(c.p_full[1]), pph1, p.timeout_ns, p.status)) {
-                            ok = false;
-                            break;
-                        }
+                        if (!wait1(c, B_(c.p_full[1]), pph1, p)) { ok = false; break; }
                         pph1 ^= 1;
                         ptx::tc_fence_after();
-                        issue_pv(1, fVp % kStages, j > 1);
-                        ptx::umma_commit(B_(c.kv_empty[fVp % kStages]));
+                        issue_pv(1, vp, j > 1);
+                        ptx::umma_commit(B_(c.v_empty[vp]));
                     }
-                    issue_s(1, fK % kStages);
+                    issue_s(1, ks);
                     ptx::umma_commit(B_(c.s_full[1]));
-                    ptx::umma_commit(B_(c.kv_empty[fK % kStages]));
+                    ptx::umma_commit(B_(c.k_empty[ks]));
                     if (j == it.n - 1) ptx::umma_commit(B_(c.q_empty));
-                    fVp = fV;
                 }
                 if (!ok) break;
-                if (!wait_bar(c, B_(c.kv_full[fVp % kStages]), (fVp / kStages) & 1, p.timeout_ns,
-                              p.status)) break;
-                if (!wait_bar(c, B_(c.p_full[0]), pph0, p.timeout_ns, p.status)) break;
+                const int tl = t - 1;  // the item's last key tile
+                const int vl = tl % kVSlots;
+                if (!wait1(c, B_(c.v_full[vl]), (tl / kVSlots) & 1, p)) break;
+                if (!wait1(c, B_(c.p_full[0]), pph0, p)) break;
                 pph0 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(0, fVp % kStages, it.n > 1);
+                issue_pv(0, vl, it.n > 1);
                 ptx::umma_commit(B_(c.o_full[0]));
-                if (!wait_bar(c, B_(c.p_full[1]), pph1, p.timeout_ns, p.status)) break;
+                if (!wait1(c, B_(c.p_full[1]), pph1, p)) break;
                 pph1 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(1, fVp % kStages, it.n > 1);
+                issue_pv(1, vl, it.n > 1);
                 ptx::umma_commit(B_(c.o_full[1]));
-                ptx::umma_commit(B_(c.kv_empty[fVp % kStages]));
+                ptx::umma_commit(B_(c.v_empty[vl]));
             }
             // every MMA issued so far must finish before TMEM and shared memory go away
             ptx::umma_commit(B_(c.teardown));
@@ -409,17 +429,24 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     sph ^= 1;
                     ptx::tc_fence_after();
                     float x[BT];
-#pragma unroll
-                    for (int cc = 0; cc < BT / 32; ++cc)
-                        ptx::tmem_ld32(tS + cc * 32, *reinterpret_cast<float(*)[32]>(&x[cc * 32]));
+                    if constexpr (BT == 128) ptx::tmem_ld128(tS, x); else ptx::tmem_ld64(tS, x);
                     if (j == it.n - 1) {
 #pragma unroll
                         for (int cidx = 0; cidx < BT; ++cidx)
                             if (cidx > row) x[cidx] = -INFINITY;
                     }
-                    float mx = x[0];
+                    // row max: independent three-input chains of 32 columns each
+                    float mxc[BT / 32];
 #pragma unroll
-                    for (int cidx = 1; cidx < BT; ++cidx) mx = fmaxf(mx, x[cidx]);
+                    for (int q = 0; q < BT / 32; ++q) {
+                        const float *xb = x + 32 * q;
+                        float a = ptx::fmax3(xb[0], xb[1], xb[2]);
+#pragma unroll
+                        for (int t = 3; t < 31; t += 2) a = ptx::fmax3(a, xb[t], xb[t + 1]);
+                        mxc[q] = fmaxf(a, xb[31]);
+                    }
+                    float mx = fmaxf(mxc[0], mxc[1]);
+                    if constexpr (BT == 128) mx = ptx::fmax3(mx, mxc[2], mxc[3]);
                     const float m_new = fmaxf(m, mx * sl2);
                     const bool need = m_new > m + 8.0f;
                     float alpha = 1.f;
@@ -427,19 +454,27 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         alpha = ptx::ex2(m - m_new);
                         m = m_new;
                     }
-                    l *= alpha;
-                    const float mb = m;
+                    // p = 2^(x*scale*log2e - m): packed FMA, MUFU ex2, packed partial sums
+                    const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+                    const uint64_t nmb = ptx::f2(-m, -m);
+                    uint64_t acc[4];
 #pragma unroll
-                    for (int cc = 0; cc < BT / 32; ++cc) {
-                        uint32_t pk[16];
+                    for (int q = 0; q < 4; ++q) acc[q] = ptx::f2(0.f, 0.f);
+                    uint32_t pk[BT / 2];
 #pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const float p0 = ptx::ex2(fmaf(x[cc * 32 + 2 * t], sl2, -mb));
-                            const float p1 = ptx::ex2(fmaf(x[cc * 32 + 2 * t + 1], sl2, -mb));
-                            l += p0 + p1;
-                            pk[t] = ptx::pack_bf16x2(p0, p1);
-                        }
-                        ptx::tmem_st16(tS + cc * 16, pk);
+                    for (int t = 0; t < BT / 2; ++t) {
+                        float e0, e1;
+                        ptx::f2_split(ptx::ffma2(ptx::f2(x[2 * t], x[2 * t + 1]), sl2x2, nmb), e0, e1);
+                        const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                        acc[t & 3] = ptx::fadd2(acc[t & 3], ptx::f2(p0, p1));
+                        pk[t] = ptx::pack_bf16x2(p0, p1);
+                    }
+                    if constexpr (BT == 128) ptx::tmem_st64(tS, pk); else ptx::tmem_st32(tS, pk);
+                    {
+                        float a0, a1;
+                        ptx::f2_split(ptx::fadd2(ptx::fadd2(acc[0], acc[1]), ptx::fadd2(acc[2], acc[3])),
+                                      a0, a1);
+                        l = l * alpha + (a0 + a1);
                     }
                     if (j > 0 && __any_sync(kFull, need)) {
 #pragma unroll 1
