@@ -10,12 +10,15 @@
 //
 // One work item = (query tile i, kv head h, pair of query heads of h's group).
 // Both heads of the pair share every K/V tile staged in shared memory, and the
-// decoded list of row (h, i).  Roles inside the 320-thread CTA:
+// decoded list of row (h, i).  Roles inside the 352-thread CTA:
 //   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax of head slot 1
-//   warp  8    scheduler + TMA producer (Q pair, then K_j into a 3-slot ring and V_j into
-//              a 2-slot ring; K is consumed first, so it gets the deeper prefetch)
+//   warp  8    scheduler + K producer (K_j into a 3-slot ring; K is consumed first, so it
+//              gets the deeper prefetch); it claims the next item early and pulls that
+//              item's Q into L2, and runs ahead into the next item's K tiles
 //   warp  9    TMEM allocator + single-thread MMA issuer
+//   warp 10    Q + V producer (the item's Q pair once the previous one is released, then
+//              V_j into a 2-slot ring)
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
 // P*V MMA reads it from tensor memory, so P never touches shared memory.
@@ -39,9 +42,10 @@
 namespace sift {
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kThreads = 352;
+constexpr int kProducerWarp = 8;   // scheduler and K loads
+constexpr int kMmaWarp = 9;        // TMEM allocator and MMA issuer
+constexpr int kVProducerWarp = 10; // Q and V loads
 constexpr int kKSlots = 3;  // K ring: K_j is consumed first, so it gets the deeper ring
 constexpr int kVSlots = 2;  // V ring
 constexpr uint32_t kTmemCols = 512;
@@ -133,7 +137,7 @@ __device__ __noinline__ bool drain_bar(uint32_t bar, uint32_t parity, uint64_t t
 // bounded wait with an inlined fast path for a phase that has already completed (a
 // call into the slow path costs hundreds of cycles on the MMA issuer's critical path)
 __device__ __forceinline__ bool wait1(Ctl &c, uint32_t bar, uint32_t parity, const AttnParams &p) {
-    return ptx::mbar_try_wait(bar, parity) || wait_bar(c, bar, parity, p.timeout_ns, p.status);
+    return ptx::mbar_test_wait(bar, parity) || wait_bar(c, bar, parity, p.timeout_ns, p.status);
 }
 
 // all lanes wait, result made warp-uniform
@@ -167,6 +171,20 @@ __device__ __forceinline__ WorkItem fetch_item(const AttnParams &p, int w) {
     it.list = (static_cast<int64_t>(it.h) * p.N + it.i) * p.rowcap;
     it.valid = 1;
     return it;
+}
+
+// entry j of the item's key-tile list (0 when j is past the end); bad sparse entries are
+// reported and replaced by the diagonal tile so that every load stays inside the prompt
+template <bool DENSE>
+__device__ __forceinline__ int list_entry(const AttnParams &p, const WorkItem &it, int j) {
+    if (j >= it.n) return 0;
+    if (DENSE) return it.first + j;
+    int idx = __ldg(p.kv_idx + it.list + j);
+    if (idx < 0 || idx > it.i || (j == it.n - 1 && idx != it.i)) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        idx = it.i;
+    }
+    return idx;
 }
 
 template <int BT, int HD, bool DENSE>
@@ -206,7 +224,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             ptx::mbar_init(B_(c.p_full[s]), G::kSoftWarps);
             ptx::mbar_init(B_(c.o_full[s]), 1);
             ptx::mbar_init(B_(c.sch_full[s]), 1);
-            ptx::mbar_init(B_(c.sch_empty[s]), 1 + 2 * G::kSoftWarps);
+            ptx::mbar_init(B_(c.sch_empty[s]), 2 + 2 * G::kSoftWarps);
         }
         ptx::mbar_init(B_(c.teardown), 1);
         ptx::mbar_init(B_(c.never), 1);
@@ -228,16 +246,15 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t tmem = c.tmem_base;
 
     if (warp == kProducerWarp) {
-        // ------------------------------------------------ scheduler + TMA producer
-        int item_k = 0, qk = 0, kf = 0, vf = 0;
+        // ------------------------------------------------ scheduler + Q/K producer
+        int item_k = 0, kf = 0;
         bool alive = true;
         const uint64_t pol_kv = ptx::policy_evict_last();   // K/V tiles are re-read by many items
-        const uint64_t pol_q = ptx::policy_evict_first();   // Q is read once per item
+        int w0 = 0;
+        if (lane == 0) w0 = atomicAdd(p.work_counter, 1);
+        WorkItem nxt = fetch_item<DENSE>(p, __shfl_sync(kFull, w0, 0));
         while (alive) {
-            int w = 0;
-            if (lane == 0) w = atomicAdd(p.work_counter, 1);
-            w = __shfl_sync(kFull, w, 0);
-            const WorkItem it = fetch_item<DENSE>(p, w);
+            const WorkItem it = nxt;
             const int slot = item_k & 1;
             if (!wait_warp(c, B_(c.sch_empty[slot]), ((item_k >> 1) & 1) ^ 1, p)) break;
             if (lane == 0) {
@@ -247,33 +264,19 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             __syncwarp();
             ++item_k;
             if (!it.valid) break;
-            if (!wait_warp(c, B_(c.q_empty), (qk & 1) ^ 1, p)) break;
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(B_(c.q_full), G::kTxQ);
+            // claim the following item now and pull its Q into L2 while this one runs
+            int w = 0;
+            if (lane == 0) w = atomicAdd(p.work_counter, 1);
+            nxt = fetch_item<DENSE>(p, __shfl_sync(kFull, w, 0));
+            if (nxt.valid && lane == 0)
                 for (int s = 0; s < 2; ++s)
                     for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
-                                              B_(c.q_full), 64 * b, it.hq0 + s, it.i * BT, pol_q);
-            }
-            ++qk;
+                        ptx::tma_prefetch_l2_3d(&tmQ, 64 * b, nxt.hq0 + s, nxt.i * BT);
             for (int jb = 0; jb < it.n && alive; jb += 32) {
-                const int j = jb + static_cast<int>(lane);
-                int my = 0;
-                if (j < it.n) {
-                    if (DENSE) {
-                        my = it.first + j;
-                    } else {
-                        my = __ldg(p.kv_idx + it.list + j);
-                        const bool bad = my < 0 || my > it.i || (j == it.n - 1 && my != it.i);
-                        if (bad) {
-                            set_status(p.status, SIFT_ERR_DEVICE_CHECK);
-                            my = it.i;
-                        }
-                    }
-                }
+                const int idx_l = list_entry<DENSE>(p, it, jb + static_cast<int>(lane));
                 const int cnt = min(32, it.n - jb);
                 for (int jj = 0; jj < cnt; ++jj) {
-                    const int idx = __shfl_sync(kFull, my, jj);
+                    const int idx = __shfl_sync(kFull, idx_l, jj);
                     const int ks = kf % kKSlots;
                     if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) {
                         alive = false;
@@ -286,6 +289,45 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                                                   B_(c.k_full[ks]), 64 * b, it.h, idx * BT, pol_kv);
                     }
                     ++kf;
+                }
+            }
+        }
+        if (c.abort && lane == 0) {
+            // unwinding: let every copy already issued land before shared memory is released
+            for (int s = 0; s < kKSlots && s < kf; ++s) {
+                const int last = s + ((kf - 1 - s) / kKSlots) * kKSlots;  // last fill of slot s
+                drain_bar(B_(c.k_full[s]), (last / kKSlots) & 1, p.timeout_ns);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kVProducerWarp) {
+        // ------------------------------------------------ Q + V producer (runs behind the K producer)
+        int item_k = 0, vf = 0, qk = 0;
+        bool alive = true;
+        const uint64_t pol_kv = ptx::policy_evict_last();
+        const uint64_t pol_q = ptx::policy_evict_first();   // Q is read once per item
+        while (alive) {
+            const int slot = item_k & 1;
+            if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
+            const WorkItem it = c.items[slot];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(B_(c.sch_empty[slot]));
+            ++item_k;
+            if (!it.valid) break;
+            if (!wait_warp(c, B_(c.q_empty), (qk & 1) ^ 1, p)) break;
+            if (lane == 0) {
+                ptx::mbar_arrive_expect_tx(B_(c.q_full), G::kTxQ);
+                for (int s = 0; s < 2; ++s)
+                    for (int b = 0; b < G::kBoxes; ++b)
+                        ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
+                                              B_(c.q_full), 64 * b, it.hq0 + s, it.i * BT, pol_q);
+            }
+            ++qk;
+            for (int jb = 0; jb < it.n && alive; jb += 32) {
+                const int idx_l = list_entry<DENSE>(p, it, jb + static_cast<int>(lane));
+                const int cnt = min(32, it.n - jb);
+                for (int jj = 0; jj < cnt; ++jj) {
+                    const int idx = __shfl_sync(kFull, idx_l, jj);
                     const int vs = vf % kVSlots;
                     if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) {
                         alive = false;
@@ -302,11 +344,6 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             }
         }
         if (c.abort && lane == 0) {
-            // unwinding: let every copy already issued land before shared memory is released
-            for (int s = 0; s < kKSlots && s < kf; ++s) {
-                const int last = s + ((kf - 1 - s) / kKSlots) * kKSlots;  // last fill of slot s
-                drain_bar(B_(c.k_full[s]), (last / kKSlots) & 1, p.timeout_ns);
-            }
             for (int s = 0; s < kVSlots && s < vf; ++s) {
                 const int last = s + ((vf - 1 - s) / kVSlots) * kVSlots;
                 drain_bar(B_(c.v_full[s]), (last / kVSlots) & 1, p.timeout_ns);
@@ -316,30 +353,45 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------ single-thread MMA issuer
+        // One thread issues both heads' MMAs in the order S0(j) | PV1(j-1) S1(j) |
+        // PV0(j) S0(j+1) | ...: the heads alternate on the tensor pipe, each one's softmax
+        // running while the other head's MMAs execute.
         if (lane == 0) {
             if (p.stall) wait_bar(c, B_(c.never), 0, p.timeout_ns, p.status);
-            int item_k = 0, qk = 0, t = 0;  // t: key tiles consumed, same order as the producer
+            int item_k = 0, qk = 0;
+            // ring positions kept incrementally (no division on the issue path): K slot and
+            // phase of the current tile, V slot and phase of the previous tile
+            int ks = 0, vs = kVSlots - 1;
+            uint32_t kph = 0, vph = 1;
             uint32_t pph0 = 0, pph1 = 0;
             const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-            auto issue_s = [&](int s, int ks) {
-                const uint32_t qa = q_s + s * G::kBoxes * G::kQBox;
-                const uint32_t kb = k_s + ks * G::kKVBytes;
+            // Descriptor bases.  The start address sits in the low 14 bits (16-byte units) and
+            // every operand lies below 227 KB, so an in-bounds byte offset is added as
+            // offset >> 4 without carrying into the other fields: one 64-bit add per MMA.
+            const uint64_t dq = ptx::sdesc_sw128(q_s, 16, 1024);
+            const uint64_t dk = ptx::sdesc_sw128(k_s, 16, 1024);
+            const uint64_t dv = ptx::sdesc_sw128(v_s, G::kKVBox, 1024);
+            auto issue_s = [&](int s, int kslot) {
+                const uint64_t qa = dq + static_cast<uint32_t>((s * G::kBoxes * G::kQBox) >> 4);
+                const uint64_t kb = dk + static_cast<uint32_t>((kslot * G::kKVBytes) >> 4);
+                const uint32_t d = s ? tS1 : tS0;
+                ptx::umma_ss_c<false>(d, qa, kb, G::kIdescS);
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) {
-                    const uint32_t off_q = (kk >> 2) * G::kQBox + (kk & 3) * 32;
-                    const uint32_t off_k = (kk >> 2) * G::kKVBox + (kk & 3) * 32;
-                    ptx::umma_ss(s ? tS1 : tS0, ptx::sdesc_sw128(qa + off_q, 16, 1024),
-                                 ptx::sdesc_sw128(kb + off_k, 16, 1024), G::kIdescS, kk > 0);
+                for (int kk = 1; kk < HD / 16; ++kk) {
+                    const uint32_t off_q = ((kk >> 2) * G::kQBox + (kk & 3) * 32) >> 4;
+                    const uint32_t off_k = ((kk >> 2) * G::kKVBox + (kk & 3) * 32) >> 4;
+                    ptx::umma_ss_c<true>(d, qa + off_q, kb + off_k, G::kIdescS);
                 }
             };
-            auto issue_pv = [&](int s, int vs, bool acc) {
-                const uint32_t vb = v_s + vs * G::kKVBytes;
+            auto issue_pv = [&](int s, int vslot, bool acc) {
+                const uint64_t vb = dv + static_cast<uint32_t>((vslot * G::kKVBytes) >> 4);
+                const uint32_t d = s ? tO1 : tO0;
+                const uint32_t a = s ? tS1 : tS0;
+                if (acc) ptx::umma_ts_c<true>(d, a, vb, G::kIdescPV);
+                else ptx::umma_ts_c<false>(d, a, vb, G::kIdescPV);
 #pragma unroll
-                for (int kk = 0; kk < BT / 16; ++kk) {
-                    ptx::umma_ts(s ? tO1 : tO0, (s ? tS1 : tS0) + kk * 8,
-                                 ptx::sdesc_sw128(vb + kk * 16 * 128, G::kKVBox, 1024),
-                                 G::kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 1; kk < BT / 16; ++kk)
+                    ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
             };
             while (!c.abort) {
                 const int slot = item_k & 1;
@@ -352,20 +404,18 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 ++qk;
                 ptx::tc_fence_after();
                 bool ok = true;
-                for (int j = 0; j < it.n; ++j, ++t) {
-                    const int ks = t % kKSlots;
-                    if (!wait1(c, B_(c.k_full[ks]), (t / kKSlots) & 1, p)) { ok = false; break; }
+                for (int j = 0; j < it.n; ++j) {
+                    if (!wait1(c, B_(c.k_full[ks]), kph, p)) { ok = false; break; }
                     ptx::tc_fence_after();
-                    const int vp = (t + kVSlots - 1) % kVSlots;  // slot of V_{j-1}
                     if (j > 0) {
-                        if (!wait1(c, B_(c.v_full[vp]), ((t - 1) / kVSlots) & 1, p) ||
+                        if (!wait1(c, B_(c.v_full[vs]), vph, p) ||
                             !wait1(c, B_(c.p_full[0]), pph0, p)) {
                             ok = false;
                             break;
                         }
                         pph0 ^= 1;
                         ptx::tc_fence_after();
-                        issue_pv(0, vp, j > 1);
+                        issue_pv(0, vs, j > 1);
                     }
                     issue_s(0, ks);
                     ptx::umma_commit(B_(c.s_full[0]));
@@ -373,29 +423,27 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         if (!wait1(c, B_(c.p_full[1]), pph1, p)) { ok = false; break; }
                         pph1 ^= 1;
                         ptx::tc_fence_after();
-                        issue_pv(1, vp, j > 1);
-                        ptx::umma_commit(B_(c.v_empty[vp]));
+                        issue_pv(1, vs, j > 1);
                     }
                     issue_s(1, ks);
                     ptx::umma_commit(B_(c.s_full[1]));
-                    ptx::umma_commit(B_(c.k_empty[ks]));
-                    if (j == it.n - 1) ptx::umma_commit(B_(c.q_empty));
+                    // advance: this tile's V becomes "previous", the K ring moves on
+                    if (++vs == kVSlots) { vs = 0; vph ^= 1; }
+                    if (++ks == kKSlots) { ks = 0; kph ^= 1; }
                 }
                 if (!ok) break;
-                const int tl = t - 1;  // the item's last key tile
-                const int vl = tl % kVSlots;
-                if (!wait1(c, B_(c.v_full[vl]), (tl / kVSlots) & 1, p)) break;
+                // vs / vph now name the item's last V tile
+                if (!wait1(c, B_(c.v_full[vs]), vph, p)) break;
                 if (!wait1(c, B_(c.p_full[0]), pph0, p)) break;
                 pph0 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(0, vl, it.n > 1);
+                issue_pv(0, vs, it.n > 1);
                 ptx::umma_commit(B_(c.o_full[0]));
                 if (!wait1(c, B_(c.p_full[1]), pph1, p)) break;
                 pph1 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(1, vl, it.n > 1);
+                issue_pv(1, vs, it.n > 1);
                 ptx::umma_commit(B_(c.o_full[1]));
-                ptx::umma_commit(B_(c.v_empty[vl]));
             }
             // every MMA issued so far must finish before TMEM and shared memory go away
             ptx::umma_commit(B_(c.teardown));
@@ -414,6 +462,11 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             const float sl2 = p.scale_log2;
             int item_k = 0;
             uint32_t sph = 0, oph = 0;
+            // The first warp of head slot 1 hands buffers back to the producers: S1(j) is the
+            // last MMA to read K_j and Q (at the item's last tile), and completes after
+            // PV1(j-1), the last reader of V_{j-1}; o_full of slot 1 covers the item's last V.
+            const bool releaser = (s == 1 && wq == 0 && lane == 0);
+            int t = 0;  // key tiles seen so far, same order as the producers and the MMA issuer
             while (true) {
                 const int slot = item_k & 1;
                 if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
@@ -427,6 +480,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 for (int j = 0; j < it.n; ++j) {
                     if (!wait_warp(c, B_(c.s_full[s]), sph, p)) { ok = false; break; }
                     sph ^= 1;
+                    if (releaser) {
+                        ptx::mbar_arrive(B_(c.k_empty[t % kKSlots]));
+                        if (j > 0) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
+                        if (j == it.n - 1) ptx::mbar_arrive(B_(c.q_empty));
+                    }
+                    ++t;
                     ptx::tc_fence_after();
                     float x[BT];
                     if constexpr (BT == 128) ptx::tmem_ld128(tS, x); else ptx::tmem_ld64(tS, x);
@@ -493,6 +552,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 if (!ok) break;
                 if (!wait_warp(c, B_(c.o_full[s]), oph, p)) break;
                 oph ^= 1;
+                if (releaser) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
                 ptx::tc_fence_after();
                 const float inv = 1.f / l;
                 const int64_t tok = static_cast<int64_t>(it.i) * BT + row;
