@@ -185,7 +185,7 @@ def host_inputs_layer0(cfg):
 def run_reference(args, cfg):
     """--impl reference: the CPU oracle on a bounded sample of the same workload."""
     import oracle
-    rank = int(os.environ.get("RANK", "0"))
+    _, rank, _ = rank_env()
     if rank != 0:
         return 0
     oracle.build()
@@ -231,6 +231,32 @@ def config_dict(cfg, args, lay):
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
+# ----------------------------------------------------------------------------- multi-rank helpers
+
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment (1, 0, 0 when absent)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest `value` over all ranks (identity without a process group).  The
+    timed region is judged by its slowest rank."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, steps: int, max_seconds: float,
+                     world: int) -> float:
+    """Replicas: every rank processes the same per-GPU workload (weak scaling), so the
+    job's throughput is all ranks' work over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / max_seconds / 1e12
+
+
 # ----------------------------------------------------------------------------- GPU leg
 
 def run_ours(args, cfg):
@@ -238,9 +264,7 @@ def run_ours(args, cfg):
     import bit_vector_guided_gb300 as sift
     from bit_vector_guided_gb300 import build as sbuild
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -311,18 +335,14 @@ def run_ours(args, cfg):
         torch.cuda.synchronize(dev)
         if dist is not None:
             dist.barrier()
-    total_ms = start.elapsed_time(stop)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist, dev)
     if int(status.item()) != 0:
         raise RuntimeError("device status " + sift.status_string(int(status.item())))
     decode_ms = [ev[s][0].elapsed_time(ev[s][1]) for s in range(args.steps)]
     layer_ms = np.array([[ev[s][1 + l].elapsed_time(ev[s][2 + l]) for l in range(L)]
                          for s in range(args.steps)])
     ms_per_step = total_ms / args.steps
-    value = world * flops_step * args.steps / (total_ms * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, args.steps, total_ms * 1e-3, world)
     kern_ms = float(layer_ms.mean())
     achieved = float(flops_layer.mean()) / (kern_ms * 1e-3) / 1e12
 
@@ -457,12 +477,8 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
     for _ in range(steps):
         step()
     torch.cuda.synchronize(dev)
-    el = time.perf_counter() - t0
-    if dist is not None:
-        t = torch.tensor([el], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        el = float(t.item())
-    return {"value": world * flops_step * steps / el / 1e12, "unit": UNIT,
+    el = max_over_ranks(time.perf_counter() - t0, dist, dev)
+    return {"value": whole_job_tflops(flops_step, steps, el, world), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": 1e3 * el / steps, "steps": steps,
             "note": "pinned host buffers; H2D of each layer's Q/K/V and D2H of its O/LSE on a "
