@@ -2,20 +2,21 @@
 // a custom kernel turns the LA/CA bit vectors into explicit tile indices) and
 // the longest-first schedule consumed by the persistent attention kernel.
 //
-// One warp decodes one (layer, kv head, query tile) row.  The candidate tiles
-// of a row arrive as 64-bit words (CA words of every earlier document of the
-// prompt, then the row's own LA word(s)); every lane sees the same word, tests
-// its own bit, and takes its output slot from the popcount of the lower lanes'
-// bits, so each 32-bit half-word is compacted with one popc and written with
-// one coalesced store.  Document metadata for up to 32 earlier documents is
-// fetched by the 32 lanes at once and broadcast with shuffles.
+// One warp decodes all rows of one (layer, kv head, document) -- or of one prompt's
+// query suffix.  Candidate tiles arrive as 64-bit words (the CA words of every earlier
+// document of the prompt, then each row's own LA word(s)); every lane sees the same
+// word, tests its own bit, and takes its output slot from the popcount of the lower
+// lanes' bits, so each 32-bit half-word is compacted with one popc and written with
+// one coalesced store.  The CA prefix is the same for every row of a document, so it
+// is compacted once per document and copied; document metadata for up to 32 earlier
+// documents, and the first LA word of up to 32 rows, are fetched by the 32 lanes at
+// once and broadcast with shuffles.
 #include "ptx.cuh"
 #include "sift_internal.h"
 
 namespace sift {
 namespace {
 
-constexpr int kDecodeWarps = 8;
 
 struct DecodeArgs {
     const int32_t *cu;
@@ -69,102 +70,168 @@ struct RowWriter {
     }
 };
 
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-decode_rows_kernel(const DecodeArgs a) {
-    const uint32_t lane = threadIdx.x & 31u;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kDecodeWarps + (threadIdx.x >> 5);
-    if (row >= a.rows) return;
-    const int i = static_cast<int>(row % a.N);
-    const int h = static_cast<int>((row / a.N) % a.Hkv);
-    const int l = static_cast<int>(row / (static_cast<int64_t>(a.N) * a.Hkv));
-    const int B = a.B;
-    const int64_t tok = static_cast<int64_t>(i) * B;
+// One warp per segment of a (layer, kv head): a document of a prompt, or a prompt's
+// query suffix.  Every row of a document shares the same CA prefix (the flagged pages
+// of the earlier documents), so the warp compacts that prefix once -- into shared
+// memory and into the document's first row -- and then writes each row as prefix +
+// its own LA tiles + the diagonal.  Suffix rows list every tile of the prompt up to
+// the diagonal.
+constexpr int kSegWarps = 4;
+constexpr int kPrefixCap = 1024;  // CA prefix entries staged in shared memory per warp
 
-    const int p = find_prompt(a.cu, a.P, tok);
-    const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
-    const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
-    bool ok = (p0 % B == 0) && (p1 % B == 0) && tok >= p0 && tok < p1 && g0 >= 0 &&
-              g0 <= g1 && g1 <= a.D;
-    RowWriter w{a.kv_idx + row * a.rowcap, 0, a.rowcap, lane};
-    if (!ok) {
-        if (lane == 0) {
-            set_status(a.status, SIFT_ERR_DEVICE_CHECK);
-            w.out[0] = i;
-            a.counts[row] = 1;
+__global__ void __launch_bounds__(kSegWarps * 32)
+decode_segments_kernel(const DecodeArgs a) {
+    __shared__ int32_t prefix_smem[kSegWarps][kPrefixCap];
+    const uint32_t lane = threadIdx.x & 31u;
+    const int wib = static_cast<int>(threadIdx.x >> 5);
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * kSegWarps + wib;
+    const int S = a.D + a.P;
+    if (w >= a.rows) return;  // rows = layers * Hkv * segments here
+    const int seg = static_cast<int>(w % S);
+    const int64_t lh = w / S;  // layer * Hkv + kv head
+    const int h = static_cast<int>(lh % a.Hkv);
+    const int l = static_cast<int>(lh / a.Hkv);
+    const int B = a.B;
+    const int64_t rowbase = lh * a.N;  // row of global tile 0 for this (layer, kv head)
+    int32_t *pre = prefix_smem[wib];
+
+    if (seg >= a.D) {
+        // ---- the query suffix of prompt p: dense over the prompt
+        const int p = seg - a.D;
+        const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
+        const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
+        if (p0 % B || p1 % B || p0 > p1 || g0 < 0 || g0 > g1 || g1 > a.D) {
+            if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+            return;
+        }
+        const int sstart = g1 > g0 ? __ldg(a.doc_end + g1 - 1) : p0;
+        if (sstart % B || sstart < p0 || sstart > p1) {
+            if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+            return;
+        }
+        const int pt = p0 / B;
+        for (int i = sstart / B; i < p1 / B; ++i) {
+            int32_t *out = a.kv_idx + (rowbase + i) * a.rowcap;
+            int n = i - pt + 1;
+            if (n > a.rowcap) {
+                if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+                n = a.rowcap;
+            }
+            for (int k = static_cast<int>(lane); k < n; k += 32) out[k] = pt + k;
+            if (lane == 0) a.counts[rowbase + i] = n;
         }
         return;
     }
-    // own document: the first one ending after tok (none -> query suffix)
-    int lo = g0, hi = g1;
+
+    // ---- document g
+    const int g = seg;
+    int lo = 0, hi = a.P - 1;  // prompt owning g: the last p with doc_cu[p] <= g
     while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(a.doc_end + mid) > tok) hi = mid; else lo = mid + 1;
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(a.doc_cu + mid) <= g) lo = mid; else hi = mid - 1;
     }
-    const int g = lo;
-    if (g == g1) {
-        // suffix row: every tile of the prompt up to the diagonal
-        const int pt = p0 / B;
-        int n = i - pt + 1;
-        if (n > a.rowcap) { if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK); n = a.rowcap; }
-        for (int k = static_cast<int>(lane); k < n; k += 32) w.out[k] = pt + k;
-        if (lane == 0) a.counts[row] = n;
+    const int p = lo;
+    const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
+    const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
+    const int ds = (g == g0) ? p0 : __ldg(a.doc_end + g - 1);
+    const int de = __ldg(a.doc_end + g);
+    if (g < g0 || g >= g1 || p0 % B || ds % B || de % B || de <= ds || ds < p0 || de > p1) {
+        if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
         return;
     }
+    const int T = (de - ds) / B;
+    const int W = (T + 63) / 64;
+    const int t0 = ds / B;
+    int32_t *row0 = a.kv_idx + (rowbase + t0) * a.rowcap;
     bool bad = false;
-    // CA pages of the earlier documents, 32 documents per round trip
+
+    // CA prefix of the earlier documents, 32 documents per round trip
+    int c = 0;  // warp-uniform
     for (int base = g0; base < g; base += 32) {
         const int gk = base + static_cast<int>(lane);
-        int ds = 0, T = 0;
-        int64_t off = 0;
+        int dsk = 0, Tk = 0;
+        int64_t offk = 0;
         uint64_t w0 = 0;
         if (gk < g) {
-            ds = (gk == g0) ? p0 : __ldg(a.doc_end + gk - 1);
-            const int de = __ldg(a.doc_end + gk);
-            T = (de - ds) / B;
-            const int W = (T + 63) / 64;
-            off = __ldg(a.ca_off + gk) + (static_cast<int64_t>(l) * a.Hkv + h) * W;
-            if (de <= ds || (de - ds) % B != 0 || ds % B != 0 || off < 0 || off + W > a.ca_len) {
+            dsk = (gk == g0) ? p0 : __ldg(a.doc_end + gk - 1);
+            const int dek = __ldg(a.doc_end + gk);
+            Tk = (dek - dsk) / B;
+            const int Wk = (Tk + 63) / 64;
+            offk = __ldg(a.ca_off + gk) + (static_cast<int64_t>(l) * a.Hkv + h) * Wk;
+            if (dek <= dsk || (dek - dsk) % B != 0 || dsk % B != 0 || offk < 0 ||
+                offk + Wk > a.ca_len) {
                 bad = true;
-                T = 0;
+                Tk = 0;
             } else {
-                w0 = __ldg(a.ca + off);
+                w0 = __ldg(a.ca + offk);
             }
         }
         const int nd = min(32, g - base);
         for (int k = 0; k < nd; ++k) {
-            const int Tk = __shfl_sync(0xffffffffu, T, k);
-            const int dsk = __shfl_sync(0xffffffffu, ds, k);
-            const int64_t offk = __shfl_sync(0xffffffffu, off, k);
-            const uint64_t wk = __shfl_sync(0xffffffffu, w0, k);
-            const int W = (Tk + 63) / 64;
-            for (int wi = 0; wi < W; ++wi) {
-                const uint64_t word = wi == 0 ? wk : __ldg(a.ca + offk + wi);
-                w.emit(word, min(64, Tk - 64 * wi), dsk / B + 64 * wi);
+            const int Tq = __shfl_sync(0xffffffffu, Tk, k);
+            const int dsq = __shfl_sync(0xffffffffu, dsk, k);
+            const int64_t offq = __shfl_sync(0xffffffffu, offk, k);
+            const uint64_t wq = __shfl_sync(0xffffffffu, w0, k);
+            const int Wq = (Tq + 63) / 64;
+            for (int wi = 0; wi < Wq; ++wi) {
+                const uint64_t word = wi == 0 ? wq : __ldg(a.ca + offq + wi);
+                const int nb = min(64, Tq - 64 * wi);
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int rem = nb - 32 * half;
+                    if (rem <= 0) break;
+                    uint32_t bits = static_cast<uint32_t>(word >> (32 * half));
+                    if (rem < 32) bits &= (1u << rem) - 1u;
+                    if (bits == 0) continue;
+                    if ((bits >> lane) & 1u) {
+                        const int pos = c + __popc(bits & ((1u << lane) - 1u));
+                        const int tile = dsq / B + 64 * wi + 32 * half + static_cast<int>(lane);
+                        if (pos < kPrefixCap) pre[pos] = tile;
+                        if (pos < a.rowcap) row0[pos] = tile;
+                    }
+                    c += __popc(bits);
+                }
             }
         }
     }
-    // LA tiles j < i of the own document
-    {
-        const int ds = (g == g0) ? p0 : __ldg(a.doc_end + g - 1);
-        const int de = __ldg(a.doc_end + g);
-        const int T = (de - ds) / B;
-        const int W = (T + 63) / 64;
-        const int il = i - ds / B;
-        const int64_t off = __ldg(a.la_off + g) + ((static_cast<int64_t>(l) * a.Hkv + h) * T + il) * W;
-        if (de <= ds || (de - ds) % B != 0 || ds % B != 0 || off < 0 || off + W > a.la_len) {
-            bad = true;
-        } else {
-            for (int wi = 0; 64 * wi < il; ++wi)
-                w.emit(__ldg(a.la + off + wi), min(64, il - 64 * wi), ds / B + 64 * wi);
+    __syncwarp();
+
+    // rows of the document: prefix, LA tiles j < il, diagonal
+    const int64_t la_base = __ldg(a.la_off + g) + (static_cast<int64_t>(l) * a.Hkv + h) * T * W;
+    if (la_base < 0 || la_base + static_cast<int64_t>(T) * W > a.la_len) bad = true;
+    bad = __any_sync(0xffffffffu, bad);  // warp-uniform from here on
+    const int cc = min(c, a.rowcap);
+    for (int rb = 0; rb < T; rb += 32) {
+        // first LA word of 32 rows in one round trip
+        const int rl = rb + static_cast<int>(lane);
+        uint64_t lw = 0;
+        if (!bad && rl < T) lw = __ldg(a.la + la_base + static_cast<int64_t>(rl) * W);
+        const int nr = min(32, T - rb);
+        for (int r = 0; r < nr; ++r) {
+            const int il = rb + r;
+            const uint64_t word0 = __shfl_sync(0xffffffffu, lw, r);
+            RowWriter wr{a.kv_idx + (rowbase + t0 + il) * a.rowcap, cc, a.rowcap, lane};
+            if (il > 0)
+                for (int k = static_cast<int>(lane); k < cc; k += 32)
+                    wr.out[k] = k < kPrefixCap ? pre[k] : row0[k];
+            wr.n = c;
+            if (!bad) {
+                for (int wi = 0; 64 * wi < il; ++wi) {
+                    const uint64_t word =
+                        wi == 0 ? word0 : __ldg(a.la + la_base + static_cast<int64_t>(il) * W + wi);
+                    wr.emit(word, min(64, il - 64 * wi), t0 + 64 * wi);
+                }
+            }
+            if (lane == 0 && wr.n < a.rowcap) wr.out[wr.n] = t0 + il;
+            wr.n += 1;
+            if (lane == 0) {
+                if (wr.n > a.rowcap) bad = true;
+                a.counts[rowbase + t0 + il] = min(wr.n, a.rowcap);
+            }
         }
     }
-    if (lane == 0 && w.n < a.rowcap) w.out[w.n] = i;
-    w.n += 1;
     bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0) {
-        if (bad || w.n > a.rowcap) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
-        a.counts[row] = min(w.n, a.rowcap);
-    }
+    if (lane == 0 && bad) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
 }
 
 // one block per group: counting sort by count, descending
@@ -283,10 +350,11 @@ extern "C" sift_status sift_decode(const sift_problem *prob, const uint64_t *la_
     a.B = prob->tile;
     a.N = prob->total_tokens / prob->tile;
     a.rowcap = prob->max_tiles_per_prompt;
-    a.rows = static_cast<int64_t>(prob->num_layers) * a.Hkv * a.N;
-    const int64_t blocks = (a.rows + kDecodeWarps - 1) / kDecodeWarps;
+    // one warp per (layer, kv head, segment), a segment being a document or a suffix
+    a.rows = static_cast<int64_t>(prob->num_layers) * a.Hkv * (a.D + a.P);
+    const int64_t blocks = (a.rows + kSegWarps - 1) / kSegWarps;
     if (blocks > INT32_MAX) return SIFT_ERR_UNSUPPORTED;
-    decode_rows_kernel<<<static_cast<unsigned>(blocks), kDecodeWarps * 32, 0, stream>>>(a);
+    decode_segments_kernel<<<static_cast<unsigned>(blocks), kSegWarps * 32, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SIFT_ERR_CUDA;
     if (launch_schedule(counts, sched, prob->num_layers, a.N * a.Hkv, a.rowcap, dev_status,
                         stream) != cudaSuccess)
