@@ -48,9 +48,13 @@ def build(force: bool = False) -> str:
 
 
 def load():
+    """The compiled oracle.  SIFT_ORACLE_LIB, when set, names another build of the same
+    source to load instead (the mutation tests point it at copies with planted
+    mistakes to show that the pins catch them)."""
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(build())
+        override = os.environ.get("SIFT_ORACLE_LIB")
+        lib = ctypes.CDLL(override if override else build())
         P = ctypes.c_void_p
         i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
         lib.sift_oracle_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, P, P]
