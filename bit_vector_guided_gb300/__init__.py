@@ -7,9 +7,9 @@ library ``libsift.so`` behind the C ABI of ``include/sift.h``; this package is
 the Python binding of that library.
 """
 from ._native import (STATUS, SiftError, SiftProblem, abi_version, debug_set_waits, decode,
-                      dense_prefill, dense_prefill_noalloc, exported_symbols, load_library, sparse_prefill,
+                      dense_prefill, dense_prefill_noalloc, exported_symbols, fused_prefill, load_library, sparse_prefill,
                       status_string, workspace_bytes)
 
 __all__ = ["STATUS", "SiftError", "SiftProblem", "abi_version", "debug_set_waits", "decode",
-           "dense_prefill", "dense_prefill_noalloc", "exported_symbols", "load_library", "sparse_prefill", "status_string",
+           "dense_prefill", "dense_prefill_noalloc", "exported_symbols", "fused_prefill", "load_library", "sparse_prefill", "status_string",
            "workspace_bytes"]

@@ -17,7 +17,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = ["SiftError", "SiftProblem", "load_library", "decode", "sparse_prefill",
-           "dense_prefill", "dense_prefill_noalloc", "workspace_bytes", "status_string", "debug_set_waits",
+           "dense_prefill", "dense_prefill_noalloc", "fused_prefill", "workspace_bytes", "status_string", "debug_set_waits",
            "abi_version", "exported_symbols", "STATUS"]
 
 STATUS = {0: "SIFT_OK", 1: "SIFT_ERR_INVALID_ARG", 2: "SIFT_ERR_UNSUPPORTED", 3: "SIFT_ERR_CUDA",
@@ -65,6 +65,8 @@ def load_library(path: Optional[str] = None):
     lib.sift_sparse_prefill.restype = i32
     lib.sift_dense_prefill.argtypes = [P, P, P, P, f32, P, P, P, sz, P, P]
     lib.sift_dense_prefill.restype = i32
+    lib.sift_fused_prefill.argtypes = [P, i32, P, P, P, P, P, f32, P, P, P, sz, P, P]
+    lib.sift_fused_prefill.restype = i32
     lib.sift_dense_prefill_noalloc.argtypes = [P, P, P, P, f32, P, P, P, P]
     lib.sift_dense_prefill_noalloc.restype = i32
     lib.sift_status_string.argtypes = [i32]
@@ -234,6 +236,29 @@ def sparse_prefill(prob: SiftProblem, layer: int, q, k, v, kv_idx, counts, sched
                                  _ptr(lse), _ptr(workspace), int(workspace.numel()),
                                  _ptr(dev_status), _stream(stream))
     _check(rc, "sift_sparse_prefill")
+    return o, lse
+
+
+def fused_prefill(prob: SiftProblem, layer: int, la_words, ca_words, q, k, v,
+                  softmax_scale: float = 0.0, o=None, lse=None, workspace=None,
+                  dev_status=None, stream=None):
+    """sift_fused_prefill: decode fused into the sparse prefill; returns (o, lse)."""
+    import torch
+    lib = load_library()
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((prob.num_q_heads, prob.total_tokens), dtype=torch.float32,
+                          device=q.device)
+    if workspace is None:
+        workspace = prob.new_workspace()
+    if dev_status is None:
+        dev_status = prob.new_status()
+    rc = lib.sift_fused_prefill(prob.ref, int(layer), _ptr(la_words), _ptr(ca_words), _ptr(q),
+                                _ptr(k), _ptr(v), float(softmax_scale), _ptr(o), _ptr(lse),
+                                _ptr(workspace), int(workspace.numel()), _ptr(dev_status),
+                                _stream(stream))
+    _check(rc, "sift_fused_prefill")
     return o, lse
 
 

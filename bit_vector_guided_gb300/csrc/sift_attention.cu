@@ -52,6 +52,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all of TMEM)
 
+// where a work item's key-tile list comes from
+constexpr int kModeList = 0;   // decoded lists in HBM (sift_sparse_prefill)
+constexpr int kModeDense = 1;  // implicit {prompt start .. i} (sift_dense_prefill)
+constexpr int kModeBits = 2;   // the LA/CA bits themselves, walked on the fly (sift_fused_prefill)
+constexpr int kMaxFusedPrompts = 64;
+
 struct WorkItem {
     int32_t valid;
     int32_t h;      // kv head
@@ -60,6 +66,14 @@ struct WorkItem {
     int32_t n;      // key tiles in the row's list
     int32_t first;  // dense rows: first tile of the prompt
     int64_t list;   // sparse rows: element offset of the row inside the kv_idx slice
+    // rows walked from the bits
+    int32_t pt;      // first tile of the prompt
+    int32_t g;       // the row's document, -1 for a suffix row
+    int32_t g0;      // first document of the prompt
+    int32_t t0;      // first tile of the row's document
+    int32_t W;       // LA words per row of the document
+    int32_t pad;
+    int64_t la_row;  // word offset of the row's LA words
 };
 
 struct Ctl {
@@ -71,6 +85,9 @@ struct Ctl {
     WorkItem items[2];
     uint32_t tmem_base;
     volatile int32_t abort;
+    // rows walked from the bits: prompts by decreasing length (rank -> prompt, tiles)
+    int32_t pord[kMaxFusedPrompts];
+    int32_t plen[kMaxFusedPrompts];
 };
 
 struct AttnParams {
@@ -85,6 +102,12 @@ struct AttnParams {
     float scale_log2;
     uint64_t timeout_ns;
     int32_t stall;
+    // rows walked from the bits (sift_fused_prefill)
+    const int32_t *cu, *doc_cu, *doc_end;
+    const int64_t *la_off, *ca_off;
+    const uint64_t *la, *ca;
+    int64_t la_len, ca_len;
+    int32_t P, D, B, layer, Hkv;
 };
 
 template <int BT, int HD>
@@ -146,8 +169,9 @@ __device__ __forceinline__ bool wait_warp(Ctl &c, uint32_t bar, uint32_t parity,
     return __all_sync(kFull, wait1(c, bar, parity, p));
 }
 
-template <bool DENSE>
+template <int MODE>
 __device__ __forceinline__ WorkItem fetch_item(const AttnParams &p, int w) {
+    constexpr bool DENSE = MODE == kModeDense;
     WorkItem it{};
     if (w >= p.total_items) return it;
     const int uidx = w / p.pairs;
@@ -175,8 +199,9 @@ __device__ __forceinline__ WorkItem fetch_item(const AttnParams &p, int w) {
 
 // entry j of the item's key-tile list (0 when j is past the end); bad sparse entries are
 // reported and replaced by the diagonal tile so that every load stays inside the prompt
-template <bool DENSE>
+template <int MODE>
 __device__ __forceinline__ int list_entry(const AttnParams &p, const WorkItem &it, int j) {
+    constexpr bool DENSE = MODE == kModeDense;
     if (j >= it.n) return 0;
     if (DENSE) return it.first + j;
     int idx = __ldg(p.kv_idx + it.list + j);
@@ -187,12 +212,177 @@ __device__ __forceinline__ int list_entry(const AttnParams &p, const WorkItem &i
     return idx;
 }
 
-template <int BT, int HD, bool DENSE>
+// ---- rows walked from the bits ------------------------------------------------------
+// Work order without a decode pass: by decreasing position inside the prompt (a row's
+// tile count grows with its position), over prompts sorted by decreasing length, then
+// kv head and head pair.  The CTA sorts the prompts once (Ctl::pord / plen).
+
+// CA pages of documents g0+32*chunk .. : lane k loads document g0+32*chunk+k's start,
+// tile count and first CA word (T = 0 for a document outside the range or malformed)
+struct CaLane {
+    int ds, T;
+    int64_t off;
+    uint64_t w0;
+};
+
+__device__ __forceinline__ CaLane ca_lane(const AttnParams &p, int p0, int g0, int g, int gk,
+                                          int h) {
+    CaLane r{0, 0, 0, 0};
+    if (gk >= g) return r;
+    r.ds = (gk == g0) ? p0 : __ldg(p.doc_end + gk - 1);
+    const int de = __ldg(p.doc_end + gk);
+    const int T = (de - r.ds) / p.B;
+    const int W = (T + 63) / 64;
+    r.off = __ldg(p.ca_off + gk) + (static_cast<int64_t>(p.layer) * p.Hkv + h) * W;
+    if (de <= r.ds || (de - r.ds) % p.B || r.ds % p.B || r.off < 0 || r.off + W > p.ca_len) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        return CaLane{0, 0, 0, 0};
+    }
+    r.T = T;
+    r.w0 = __ldg(p.ca + r.off);
+    return r;
+}
+
+__device__ __forceinline__ uint64_t low_bits(uint64_t word, int nb) {
+    return nb >= 64 ? word : (nb <= 0 ? 0ull : (word & ((1ull << nb) - 1ull)));
+}
+
+// warp-collective: the item for work index w, with its tile count taken from the bits
+__device__ WorkItem fetch_item_bits(const AttnParams &p, const Ctl &c, int w, uint32_t lane) {
+    WorkItem it{};
+    if (w >= p.total_items) return it;
+    const int HP = p.Hkv * p.pairs;
+    int64_t base = 0;
+    int x = 0, rank = 0, rest = 0;
+    bool found = false;
+    for (int sgm = 0; sgm < p.P && !found; ++sgm) {
+        const int lo = sgm + 1 < p.P ? c.plen[sgm + 1] : 0;
+        const int64_t per = static_cast<int64_t>(sgm + 1) * HP;  // items per position
+        const int64_t cnt = static_cast<int64_t>(c.plen[sgm] - lo) * per;
+        if (w < base + cnt) {
+            const int64_t off = w - base;
+            x = c.plen[sgm] - 1 - static_cast<int>(off / per);
+            const int r = static_cast<int>(off % per);
+            rank = r / HP;
+            rest = r % HP;
+            found = true;
+        }
+        base += cnt;
+    }
+    if (!found) return it;  // the prompt lengths do not add up: nothing to do
+    const int pr = c.pord[rank];
+    it.h = rest / p.pairs;
+    const int pair = rest % p.pairs;
+    it.hq0 = it.h * p.G + 2 * pair;
+    const int B = p.B;
+    const int p0 = __ldg(p.cu + pr);
+    it.pt = p0 / B;
+    it.i = it.pt + x;
+    it.g0 = __ldg(p.doc_cu + pr);
+    int g1 = __ldg(p.doc_cu + pr + 1);
+    if (it.g0 < 0 || it.g0 > g1 || g1 > p.D) {  // malformed: treat the prompt as all suffix
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        it.g0 = g1 = 0;
+    }
+    // document of tile i: the first one ending after it (none: the query suffix)
+    int lo = it.g0, hi = g1;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.doc_end + mid) > it.i * B) hi = mid; else lo = mid + 1;
+    }
+    it.valid = 1;
+    if (lo == g1) {
+        it.g = -1;
+        it.n = x + 1;
+        return it;
+    }
+    it.g = lo;
+    const int ds = (lo == it.g0) ? p0 : __ldg(p.doc_end + lo - 1);
+    const int de = __ldg(p.doc_end + lo);
+    const int T = (de - ds) / B;
+    it.W = (T + 63) / 64;
+    it.t0 = ds / B;
+    const int il = it.i - it.t0;
+    it.la_row = __ldg(p.la_off + lo) +
+                ((static_cast<int64_t>(p.layer) * p.Hkv + it.h) * T + il) * it.W;
+    int n = 1;  // the diagonal
+    for (int b0 = it.g0; b0 < it.g; b0 += 32) {
+        const CaLane cl = ca_lane(p, p0, it.g0, it.g, b0 + static_cast<int>(lane), it.h);
+        int cnt = 0;
+        const int Wk = (cl.T + 63) / 64;
+        for (int wi = 0; wi < Wk; ++wi)
+            cnt += __popcll(low_bits(wi == 0 ? cl.w0 : __ldg(p.ca + cl.off + wi), cl.T - 64 * wi));
+        n += __reduce_add_sync(kFull, cnt);
+    }
+    if (de <= ds || (de - ds) % B || ds % B || it.la_row < 0 ||
+        it.la_row + it.W > p.la_len) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        it.W = 0;  // no LA words
+    }
+    int cnt = 0;
+    for (int wi = static_cast<int>(lane); wi < it.W && 64 * wi < il; wi += 32)
+        cnt += __popcll(low_bits(__ldg(p.la + it.la_row + wi), il - 64 * wi));
+    n += __reduce_add_sync(kFull, cnt);
+    it.n = min(n, p.rowcap);
+    return it;
+}
+
+// warp-collective: visit(j) for every key tile of the item in ascending order -- CA pages
+// of the earlier documents, LA tiles below the diagonal, the diagonal -- exactly it.n
+// times; returns false as soon as visit does
+template <typename F>
+__device__ bool walk_bits(const AttnParams &p, const WorkItem &it, uint32_t lane, F &&visit) {
+    if (it.g < 0) {
+        for (int j = it.pt; j <= it.i; ++j)
+            if (!visit(j)) return false;
+        return true;
+    }
+    int done = 0;
+    const int limit = it.n - 1;  // tiles before the diagonal
+    const int p0 = it.pt * p.B;
+    for (int b0 = it.g0; b0 < it.g && done < limit; b0 += 32) {
+        const CaLane cl = ca_lane(p, p0, it.g0, it.g, b0 + static_cast<int>(lane), it.h);
+        const int nd = min(32, it.g - b0);
+        for (int k = 0; k < nd && done < limit; ++k) {
+            const int Tq = __shfl_sync(kFull, cl.T, k);
+            const int dsq = __shfl_sync(kFull, cl.ds, k);
+            const int64_t offq = __shfl_sync(kFull, cl.off, k);
+            const uint64_t wq = __shfl_sync(kFull, cl.w0, k);
+            const int Wq = (Tq + 63) / 64;
+            for (int wi = 0; wi < Wq && done < limit; ++wi) {
+                uint64_t word = low_bits(wi == 0 ? wq : __ldg(p.ca + offq + wi), Tq - 64 * wi);
+                while (word && done < limit) {
+                    const int b = __ffsll(static_cast<long long>(word)) - 1;
+                    word &= word - 1;
+                    ++done;
+                    if (!visit(dsq / p.B + 64 * wi + b)) return false;
+                }
+            }
+        }
+    }
+    const int il = it.i - it.t0;
+    for (int wi = 0; wi < it.W && 64 * wi < il && done < limit; ++wi) {
+        uint64_t word = low_bits(__ldg(p.la + it.la_row + wi), il - 64 * wi);
+        while (word && done < limit) {
+            const int b = __ffsll(static_cast<long long>(word)) - 1;
+            word &= word - 1;
+            ++done;
+            if (!visit(it.t0 + 64 * wi + b)) return false;
+        }
+    }
+    for (; done < limit; ++done)  // only on malformed input (reported at fetch time)
+        if (!visit(it.i)) return false;
+    return visit(it.i);
+}
+
+template <int BT, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using G = Geo<BT, HD>;
+    constexpr bool DENSE = MODE == kModeDense;
+    (void)DENSE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
@@ -229,6 +419,20 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         ptx::mbar_init(B_(c.teardown), 1);
         ptx::mbar_init(B_(c.never), 1);
         c.abort = 0;
+        if (MODE == kModeBits) {
+            // prompts by decreasing tile count (insertion sort; at most 64 prompts)
+            for (int q = 0; q < p.P; ++q) {
+                const int len = (__ldg(p.cu + q + 1) - __ldg(p.cu + q)) / p.B;
+                int r = q;
+                while (r > 0 && c.plen[r - 1] < len) {
+                    c.plen[r] = c.plen[r - 1];
+                    c.pord[r] = c.pord[r - 1];
+                    --r;
+                }
+                c.plen[r] = len < 0 ? 0 : len;
+                c.pord[r] = q;
+            }
+        }
         ptx::fence_mbar_init();
     }
     if (warp == kProducerWarp && lane == 0) {
@@ -252,7 +456,11 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         const uint64_t pol_kv = ptx::policy_evict_last();   // K/V tiles are re-read by many items
         int w0 = 0;
         if (lane == 0) w0 = atomicAdd(p.work_counter, 1);
-        WorkItem nxt = fetch_item<DENSE>(p, __shfl_sync(kFull, w0, 0));
+        auto fetch = [&](int w) {
+            if constexpr (MODE == kModeBits) return fetch_item_bits(p, c, w, lane);
+            else return fetch_item<MODE>(p, w);
+        };
+        WorkItem nxt = fetch(__shfl_sync(kFull, w0, 0));
         while (alive) {
             const WorkItem it = nxt;
             const int slot = item_k & 1;
@@ -267,28 +475,31 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             // claim the following item now and pull its Q into L2 while this one runs
             int w = 0;
             if (lane == 0) w = atomicAdd(p.work_counter, 1);
-            nxt = fetch_item<DENSE>(p, __shfl_sync(kFull, w, 0));
+            nxt = fetch(__shfl_sync(kFull, w, 0));
             if (nxt.valid && lane == 0)
                 for (int s = 0; s < 2; ++s)
                     for (int b = 0; b < G::kBoxes; ++b)
                         ptx::tma_prefetch_l2_3d(&tmQ, 64 * b, nxt.hq0 + s, nxt.i * BT);
-            for (int jb = 0; jb < it.n && alive; jb += 32) {
-                const int idx_l = list_entry<DENSE>(p, it, jb + static_cast<int>(lane));
-                const int cnt = min(32, it.n - jb);
-                for (int jj = 0; jj < cnt; ++jj) {
-                    const int idx = __shfl_sync(kFull, idx_l, jj);
-                    const int ks = kf % kKSlots;
-                    if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) {
-                        alive = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
-                        for (int b = 0; b < G::kBoxes; ++b)
-                            ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox, &tmK,
-                                                  B_(c.k_full[ks]), 64 * b, it.h, idx * BT, pol_kv);
-                    }
-                    ++kf;
+            auto load_k = [&](int idx) -> bool {
+                const int ks = kf % kKSlots;
+                if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
+                    for (int b = 0; b < G::kBoxes; ++b)
+                        ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox, &tmK,
+                                              B_(c.k_full[ks]), 64 * b, it.h, idx * BT, pol_kv);
+                }
+                ++kf;
+                return true;
+            };
+            if constexpr (MODE == kModeBits) {
+                alive = walk_bits(p, it, lane, load_k);
+            } else {
+                for (int jb = 0; jb < it.n && alive; jb += 32) {
+                    const int idx_l = list_entry<MODE>(p, it, jb + static_cast<int>(lane));
+                    const int cnt = min(32, it.n - jb);
+                    for (int jj = 0; jj < cnt && alive; ++jj)
+                        alive = load_k(__shfl_sync(kFull, idx_l, jj));
                 }
             }
         }
@@ -323,23 +534,26 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                                               B_(c.q_full), 64 * b, it.hq0 + s, it.i * BT, pol_q);
             }
             ++qk;
-            for (int jb = 0; jb < it.n && alive; jb += 32) {
-                const int idx_l = list_entry<DENSE>(p, it, jb + static_cast<int>(lane));
-                const int cnt = min(32, it.n - jb);
-                for (int jj = 0; jj < cnt; ++jj) {
-                    const int idx = __shfl_sync(kFull, idx_l, jj);
-                    const int vs = vf % kVSlots;
-                    if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) {
-                        alive = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
-                        for (int b = 0; b < G::kBoxes; ++b)
-                            ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox, &tmV,
-                                                  B_(c.v_full[vs]), 64 * b, it.h, idx * BT, pol_kv);
-                    }
-                    ++vf;
+            auto load_v = [&](int idx) -> bool {
+                const int vs = vf % kVSlots;
+                if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) return false;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
+                    for (int b = 0; b < G::kBoxes; ++b)
+                        ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox, &tmV,
+                                              B_(c.v_full[vs]), 64 * b, it.h, idx * BT, pol_kv);
+                }
+                ++vf;
+                return true;
+            };
+            if constexpr (MODE == kModeBits) {
+                alive = walk_bits(p, it, lane, load_v);
+            } else {
+                for (int jb = 0; jb < it.n && alive; jb += 32) {
+                    const int idx_l = list_entry<MODE>(p, it, jb + static_cast<int>(lane));
+                    const int cnt = min(32, it.n - jb);
+                    for (int jj = 0; jj < cnt && alive; ++jj)
+                        alive = load_v(__shfl_sync(kFull, idx_l, jj));
                 }
             }
         }
@@ -622,11 +836,11 @@ bool make_map(CUtensorMap *m, const void *base, int d, int heads, int tokens, in
            CUDA_SUCCESS;
 }
 
-template <int BT, int HD, bool DENSE>
+template <int BT, int HD, int MODE>
 sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
                              const AttnParams &p, cudaStream_t stream) {
     using G = Geo<BT, HD>;
-    auto kern = sift_attention_kernel<BT, HD, DENSE>;
+    auto kern = sift_attention_kernel<BT, HD, MODE>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -642,13 +856,13 @@ sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const
     return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
 }
 
-template <bool DENSE>
+template <int MODE>
 sift_status dispatch(int tile, int hd, const CUtensorMap &mq, const CUtensorMap &mk,
                      const CUtensorMap &mv, const AttnParams &p, cudaStream_t stream) {
-    if (tile == 128 && hd == 128) return launch_attention<128, 128, DENSE>(mq, mk, mv, p, stream);
-    if (tile == 128 && hd == 64) return launch_attention<128, 64, DENSE>(mq, mk, mv, p, stream);
-    if (tile == 64 && hd == 128) return launch_attention<64, 128, DENSE>(mq, mk, mv, p, stream);
-    if (tile == 64 && hd == 64) return launch_attention<64, 64, DENSE>(mq, mk, mv, p, stream);
+    if (tile == 128 && hd == 128) return launch_attention<128, 128, MODE>(mq, mk, mv, p, stream);
+    if (tile == 128 && hd == 64) return launch_attention<128, 64, MODE>(mq, mk, mv, p, stream);
+    if (tile == 64 && hd == 128) return launch_attention<64, 128, MODE>(mq, mk, mv, p, stream);
+    if (tile == 64 && hd == 64) return launch_attention<64, 64, MODE>(mq, mk, mv, p, stream);
     return SIFT_ERR_UNSUPPORTED;
 }
 
@@ -720,7 +934,7 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
     p.counts = counts + lu;
     p.sched = sched + lu;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<false>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeList>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
 }
 
 extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const void *k,
@@ -744,5 +958,43 @@ extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *
     p.counts = ws_counts;
     p.sched = ws_sched;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<true>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeDense>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+}
+
+extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t layer,
+                                          const uint64_t *la_words, const uint64_t *ca_words,
+                                          const void *q, const void *k, const void *v,
+                                          float softmax_scale, void *o, float *lse,
+                                          void *workspace, size_t workspace_bytes,
+                                          int32_t *dev_status, cudaStream_t stream) {
+    using namespace sift;
+    if (prob == nullptr || layer < 0 || layer >= prob->num_layers) return SIFT_ERR_INVALID_ARG;
+    if ((prob->la_words_len > 0 && la_words == nullptr) ||
+        (prob->ca_words_len > 0 && ca_words == nullptr))
+        return SIFT_ERR_INVALID_ARG;
+    if (prob->num_prompts > kMaxFusedPrompts) return SIFT_ERR_UNSUPPORTED;
+    CUtensorMap maps[3];
+    AttnParams p;
+    sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
+                             dev_status, maps, &p);
+    if (st != SIFT_OK) return st;
+    p.kv_idx = nullptr;
+    p.counts = nullptr;
+    p.sched = nullptr;
+    p.cu = prob->cu_seqlens;
+    p.doc_cu = prob->doc_cu;
+    p.doc_end = prob->doc_end;
+    p.la_off = prob->la_off;
+    p.ca_off = prob->ca_off;
+    p.la = la_words;
+    p.ca = ca_words;
+    p.la_len = prob->la_words_len;
+    p.ca_len = prob->ca_words_len;
+    p.P = prob->num_prompts;
+    p.D = prob->num_docs;
+    p.B = prob->tile;
+    p.layer = layer;
+    p.Hkv = prob->num_kv_heads;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
+    return dispatch<kModeBits>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
 }

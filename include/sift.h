@@ -144,6 +144,25 @@ sift_status sift_sparse_prefill(const sift_problem *prob, int32_t layer, const v
                                 int32_t *dev_status, cudaStream_t stream);
 
 /*
+ * Decode fused into the prefill (SIFT pages, "Dettagli di Implementazione": the
+ * bits become tile indices, the sparse kernel iterates over them): one launch
+ * that walks the LA/CA words of each row on the fly and turns every set bit into
+ * a tile load, with no kv_idx list in memory and no separate decode.  Same
+ * result as sift_decode followed by sift_sparse_prefill (the same MMAs on the
+ * same tiles in the same order); rows are taken longest-first by their position
+ * in the prompt instead of by a decoded count.
+ *   la_words, ca_words: the bit words of sift_decode (all layers); `layer` picks one
+ *   q, k, v, o, lse, workspace, dev_status: as for sift_sparse_prefill
+ * At most 64 prompts per batch (SIFT_ERR_UNSUPPORTED beyond).  One memset and one
+ * kernel launch.
+ */
+sift_status sift_fused_prefill(const sift_problem *prob, int32_t layer, const uint64_t *la_words,
+                               const uint64_t *ca_words, const void *q, const void *k,
+                               const void *v, float softmax_scale, void *o, float *lse,
+                               void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                               cudaStream_t stream);
+
+/*
  * Dense causal grouped-query flash attention over each whole prompt: the full
  * recompute baseline of the SIFT pages ("Risultati").  Same kernel as
  * sift_sparse_prefill with the implicit list {prompt start .. i}; the bit
