@@ -228,7 +228,8 @@ def config_dict(cfg, args, lay):
             "docs": lay.num_docs,
             "l2": "inputs larger than L2: each layer's Q/K/V/O (> 129 MB) is distinct and "
                   "the step cycles through every layer",
-            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+            "parallelism": (f"kv-head shards x{args.gpus}" if args.shard == "heads" else
+                            f"replicas x{args.gpus}") if args.gpus > 1 else "single GPU"}
 
 
 # ----------------------------------------------------------------------------- multi-rank helpers
@@ -247,6 +248,16 @@ def max_over_ranks(value: float, dist, device) -> float:
     import torch
     t = torch.tensor([float(value)], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, dist, device) -> float:
+    """Sum of `value` over all ranks (identity without a process group)."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
     return float(t.item())
 
 
@@ -280,11 +291,30 @@ def run_ours(args, cfg):
 
     lay = W.make_layout(cfg)
     la, ca = W.make_bits(cfg, lay)
+    L = cfg.num_layers
+    shard = args.shard == "heads" and world > 1
+    if shard:
+        # this rank's kv heads (and their query heads) as an independent problem
+        import dataclasses
+        from bit_vector_guided_gb300.sharding import kv_head_range, shard_bits
+        full = cfg
+        h0, h1 = kv_head_range(rank, world, full.num_kv_heads)
+        G = full.num_q_heads // full.num_kv_heads
+        cfg = dataclasses.replace(full, num_q_heads=(h1 - h0) * G, num_kv_heads=h1 - h0)
+        la_off, ca_off, la, ca = shard_bits(lay.cu_seqlens, lay.doc_cu, lay.doc_end, lay.la_off,
+                                            lay.ca_off, la, ca, L, full.num_kv_heads,
+                                            full.tile, h0, h1)
+        lay = dataclasses.replace(lay, num_q_heads=cfg.num_q_heads,
+                                  num_kv_heads=cfg.num_kv_heads, la_off=la_off, ca_off=ca_off,
+                                  la_words_len=len(la), ca_words_len=len(ca))
+        sl = ((h0 * G, h1 * G), (h0, h1), (h0, h1))
+        qkv = [tuple(t[:, a:b].contiguous() for t, (a, b) in zip(W.make_qkv(full, l, device=dev), sl))
+               for l in range(L)]
+    else:
+        qkv = [W.make_qkv(cfg, l, device=dev) for l in range(L)]
     prob = sift.SiftProblem.from_layout(lay, dev)
     la_d = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).to(dev)
     ca_d = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).to(dev)
-    L = cfg.num_layers
-    qkv = [W.make_qkv(cfg, l, device=dev) for l in range(L)]
     outs = [(torch.empty_like(q), torch.empty((cfg.num_q_heads, lay.total_tokens),
                                               dtype=torch.float32, device=dev))
             for q, _, _ in qkv]
@@ -342,7 +372,11 @@ def run_ours(args, cfg):
     layer_ms = np.array([[ev[s][1 + l].elapsed_time(ev[s][2 + l]) for l in range(L)]
                          for s in range(args.steps)])
     ms_per_step = total_ms / args.steps
-    value = whole_job_tflops(flops_step, args.steps, total_ms * 1e-3, world)
+    if shard:  # strong scaling: the ranks' shards add up to one problem
+        job_flops_step = sum_over_ranks(flops_step, dist, dev)
+    else:      # replicas: every rank runs the whole workload
+        job_flops_step = world * flops_step
+    value = whole_job_tflops(job_flops_step, args.steps, total_ms * 1e-3, 1)
     kern_ms = float(layer_ms.mean())
     achieved = float(flops_layer.mean()) / (kern_ms * 1e-3) / 1e12
 
@@ -385,8 +419,8 @@ def run_ours(args, cfg):
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": config_dict(cfg, args, lay),
+        "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(cfg, args, lay),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sift_sparse_prefill",
@@ -409,7 +443,7 @@ def run_ours(args, cfg):
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched,
-                                status, ws, stream, dev, flops_step, world, dist)
+                                status, ws, stream, dev, job_flops_step, dist)
     if not args.no_sweep and rank == 0 and world == 1:
         result["density_sweep"] = run_sweep(args, dev, stream)
     del qkv, outs
@@ -433,7 +467,7 @@ def run_ours(args, cfg):
 
 
 def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, status, ws, stream,
-            dev, flops_step, world, dist):
+            dev, job_flops_step, dist):
     """Same metric through the public API with host buffers: every step copies that step's
     inputs (bits of all layers + Q/K/V of every layer) from pinned host memory and reads
     every layer's O and LSE back to pinned host memory."""
@@ -450,24 +484,26 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
     h2d = (la_h.numel() + ca_h.numel()) * 8 + sum(t.numel() * t.element_size()
                                                   for tri in host_in for t in tri)
     d2h = sum(o.numel() * o.element_size() + s.numel() * s.element_size() for o, s in host_out)
-    copy = torch.cuda.Stream(dev)
+    up = torch.cuda.Stream(dev)    # host -> device
+    down = torch.cuda.Stream(dev)  # device -> host, so both directions of the link overlap
     done_in = [torch.cuda.Event() for _ in range(L)]
     done_kern = [torch.cuda.Event() for _ in range(L)]
 
     def step():
-        # copies on a side stream overlap with the kernels of earlier layers; a step's
-        # uploads wait for the previous step's kernels (they overwrite the same buffers)
-        copy.wait_stream(stream)
-        with torch.cuda.stream(copy):
+        # uploads run ahead of the kernels of earlier layers; a step's uploads wait for the
+        # previous step's kernels and read-backs (they reuse the same buffers)
+        up.wait_stream(stream)
+        up.wait_stream(down)
+        with torch.cuda.stream(up):
             la_d.copy_(la_h, non_blocking=True)
             ca_d.copy_(ca_h, non_blocking=True)
         ev_bits = torch.cuda.Event()
-        ev_bits.record(copy)
+        ev_bits.record(up)
         for l in range(L):
-            with torch.cuda.stream(copy):
+            with torch.cuda.stream(up):
                 for dst, src in zip(qkv[l], host_in[l]):
                     dst.copy_(src, non_blocking=True)
-                done_in[l].record(copy)
+                done_in[l].record(up)
         stream.wait_event(ev_bits)
         sift.decode(prob, la_d, ca_d, kv_idx, counts, sched, dev_status=status, stream=stream)
         for l in range(L):
@@ -477,11 +513,12 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
             sift.sparse_prefill(prob, l, q, k, v, kv_idx, counts, sched, 0.0, o, lse, ws,
                                 status, stream)
             done_kern[l].record(stream)
-            with torch.cuda.stream(copy):
-                copy.wait_event(done_kern[l])
+            with torch.cuda.stream(down):
+                down.wait_event(done_kern[l])
                 host_out[l][0].copy_(o, non_blocking=True)
                 host_out[l][1].copy_(lse, non_blocking=True)
-        stream.wait_stream(copy)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
 
     for _ in range(max(1, min(args.warmup, 2))):
         step()
@@ -494,11 +531,11 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
         step()
     torch.cuda.synchronize(dev)
     el = max_over_ranks(time.perf_counter() - t0, dist, dev)
-    return {"value": whole_job_tflops(flops_step, steps, el, world), "unit": UNIT,
+    return {"value": whole_job_tflops(job_flops_step, steps, el, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": 1e3 * el / steps, "steps": steps,
-            "note": "pinned host buffers; H2D of each layer's Q/K/V and D2H of its O/LSE on a "
-                    "copy stream overlapping the kernels"}
+            "note": "pinned host buffers; H2D of each layer's Q/K/V on one copy stream and "
+                    "D2H of its O/LSE on another, both overlapping the kernels"}
 
 
 def run_sweep(args, dev, stream):
@@ -559,6 +596,9 @@ def main(argv=None):
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: every rank runs the whole workload (replicas, weak scaling) "
+                         "or one range of kv heads of it (heads, strong scaling)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of the workload (the JSON "
                          "line then names the reduced workload)")
