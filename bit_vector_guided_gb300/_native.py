@@ -17,7 +17,8 @@ import numpy as np
 from . import build as _build
 
 __all__ = ["SiftError", "SiftProblem", "load_library", "decode", "sparse_prefill",
-           "dense_prefill", "dense_prefill_noalloc", "fused_prefill", "workspace_bytes", "status_string", "debug_set_waits",
+           "dense_prefill", "dense_prefill_noalloc", "fused_prefill", "build_bits",
+           "build_bits_workspace_bytes", "workspace_bytes", "status_string", "debug_set_waits",
            "abi_version", "exported_symbols", "STATUS"]
 
 STATUS = {0: "SIFT_OK", 1: "SIFT_ERR_INVALID_ARG", 2: "SIFT_ERR_UNSUPPORTED", 3: "SIFT_ERR_CUDA",
@@ -69,6 +70,10 @@ def load_library(path: Optional[str] = None):
     lib.sift_fused_prefill.restype = i32
     lib.sift_dense_prefill_noalloc.argtypes = [P, P, P, P, f32, P, P, P, P]
     lib.sift_dense_prefill_noalloc.restype = i32
+    lib.sift_build_bits_workspace_bytes.argtypes = [P, i32]
+    lib.sift_build_bits_workspace_bytes.restype = sz
+    lib.sift_build_bits.argtypes = [P, i32, P, P, i32, f32, f32, f32, P, P, P, sz, P, P]
+    lib.sift_build_bits.restype = i32
     lib.sift_status_string.argtypes = [i32]
     lib.sift_status_string.restype = ctypes.c_char_p
     lib.sift_debug_set_waits.argtypes = [u64, i32]
@@ -301,3 +306,27 @@ def dense_prefill_noalloc(prob: SiftProblem, q, k, v, softmax_scale: float = 0.0
                                         _ptr(o), _ptr(lse), _ptr(dev_status), _stream(stream))
     _check(rc, "sift_dense_prefill_noalloc")
     return o, lse
+
+
+def build_bits_workspace_bytes(prob: SiftProblem, max_doc_tiles: int) -> int:
+    return int(load_library().sift_build_bits_workspace_bytes(prob.ref, int(max_doc_tiles)))
+
+
+def build_bits(prob: SiftProblem, layer: int, q, k, max_doc_tiles: int, la_fraction: float,
+               ca_fraction: float, la_words, ca_words, softmax_scale: float = 0.0,
+               workspace=None, dev_status=None, stream=None):
+    """sift_build_bits: writes layer `layer`'s LA / CA words of every document into
+    la_words / ca_words (int64 device tensors of the sizes the problem names)."""
+    import torch
+    lib = load_library()
+    if workspace is None:
+        n = (build_bits_workspace_bytes(prob, max_doc_tiles) + 15) // 16 * 16
+        workspace = torch.empty(max(n, 16), dtype=torch.uint8, device=prob.device)
+    if dev_status is None:
+        dev_status = prob.new_status()
+    rc = lib.sift_build_bits(prob.ref, int(layer), _ptr(q), _ptr(k), int(max_doc_tiles),
+                             float(la_fraction), float(ca_fraction), float(softmax_scale),
+                             _ptr(la_words), _ptr(ca_words), _ptr(workspace),
+                             int(workspace.numel()), _ptr(dev_status), _stream(stream))
+    _check(rc, "sift_build_bits")
+    return la_words, ca_words

@@ -198,6 +198,47 @@ sift_status sift_dense_prefill_noalloc(const sift_problem *prob, const void *q, 
                                        const void *v, float softmax_scale, void *o, float *lse,
                                        int32_t *dev_status, cudaStream_t stream);
 
+/*
+ * Offline construction of one layer's LA and CA bit vectors (SIFT pages,
+ * "Design del Sistema": each document is prefilled densely on its own once,
+ * the tiles and pages that draw high attention are found and stored as bits).
+ * The pages name no selection rule; this library's rule, per document, kv head
+ * h and the document's own tiles (T of them):
+ *   - tile mass M[i][j] = sum over the query heads of h's group and the B rows
+ *     of query tile i of the attention probability on the keys of tile j, from
+ *     a causal prefill of the document alone (j <= i);
+ *   - LA row i: the top ceil(la_fraction * i - 1e-4) tiles j < i by M[i][j]
+ *     (the diagonal is implicit and never written; bits at j >= i are zero);
+ *   - CA: the top ceil(ca_fraction * T - 1e-4) pages j by the mean mass they
+ *     receive, sum over i >= j of M[i][j] / (T - j);
+ *   - counts in float32 with each operation rounded on its own; ties go to
+ *     the lower index; masses come from the bf16 dense kernel, so tiles of
+ *     nearly equal mass may swap against an exact computation.
+ *   prob:           the attention problem (device arrays as for sift_decode);
+ *                   its la_off, ca_off, la_words_len, ca_words_len say where
+ *                   the words go; the documents' queries and keys are the
+ *                   prompt's own rows in q and k
+ *   layer:          which layer's words to write (q and k are that layer's)
+ *   q, k:           bf16 [total_tokens][heads][head_dim], as for the prefill
+ *   max_doc_tiles:  upper bound on any document's tile count (1 ..
+ *                   max_tiles_per_prompt); sizes the workspace
+ *   la_fraction, ca_fraction: in [0, 1]
+ *   softmax_scale:  0 selects 1/sqrt(head_dim)
+ *   la_words, ca_words: device, written only at this layer's blocks
+ *   workspace:      device, >= sift_build_bits_workspace_bytes(), 16-byte aligned
+ * A document longer than max_doc_tiles, or offsets outside the word arrays,
+ * set SIFT_ERR_DEVICE_CHECK in dev_status; those words are not written.  A
+ * batch without documents returns SIFT_OK and enqueues nothing.
+ * Launches: 1 + ceil(max_doc_tiles / head_dim) x (2 + the three of
+ * sift_dense_prefill) + 1.
+ */
+size_t sift_build_bits_workspace_bytes(const sift_problem *prob, int32_t max_doc_tiles);
+sift_status sift_build_bits(const sift_problem *prob, int32_t layer, const void *q, const void *k,
+                            int32_t max_doc_tiles, float la_fraction, float ca_fraction,
+                            float softmax_scale, uint64_t *la_words, uint64_t *ca_words,
+                            void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                            cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char *sift_status_string(sift_status status);
 

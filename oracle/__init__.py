@@ -13,6 +13,10 @@ Two independent restatements of the same definition live here:
     to an explicit token mask and dense softmax attention is taken with
     ``-inf`` outside it -- only for tiny inputs.
 
+:func:`build_bits` restates the offline step (each document prefilled alone, its
+tile masses ranked into LA/CA bits) in fp64 numpy; the pages give no selection
+rule, so the rule there is this library's reading.
+
 See ``sift_oracle.c`` for the readings of the pages (gist.science/it/paper/
 2606.09441, "Design del Sistema", "Dettagli di Implementazione") and the pins.
 """
@@ -32,7 +36,8 @@ _LIB = os.path.join(_HERE, "_build", "libsift_oracle.so")
 _lib = None
 
 __all__ = ["build", "load", "decode", "schedule", "attention_rows", "attention_all",
-           "key_mask", "brute_force_attention", "tile_mask", "set_threads"]
+           "key_mask", "brute_force_attention", "tile_mask", "set_threads",
+           "doc_tile_masses", "top_count", "select_top", "build_bits"]
 
 
 def build(force: bool = False) -> str:
@@ -254,3 +259,75 @@ def brute_force_attention(layout, la_words, ca_words, layer, q, k, v, scale=None
             O[:, qh, :] = (P / l) @ vf[:, h, :]
             LSE[qh] = (m + np.log(l))[:, 0]
     return O, LSE
+
+
+# --------------------------------------------------------------------------------------
+# Offline bit building (the step before the online path), restated in fp64 numpy.
+# --------------------------------------------------------------------------------------
+
+def doc_tile_masses(q, k, start, end, h, G, tile, scale):
+    """M[i][j]: attention probability mass that the query rows of tile i (all query heads
+    of kv head h's group) put on key tile j, in causal attention inside the document
+    [start, end) alone.  Rows of M sum to G*tile."""
+    qf = np.asarray(_bf16_bits(q[start:end, h * G:(h + 1) * G]).astype(np.uint32) << 16
+                    ).view(np.float32).astype(np.float64)
+    kf = np.asarray(_bf16_bits(k[start:end, h:h + 1]).astype(np.uint32) << 16
+                    ).view(np.float32).astype(np.float64)[:, 0]
+    n = end - start
+    T = n // tile
+    causal = np.tril(np.ones((n, n), bool))
+    M = np.zeros((T, T))
+    for g in range(G):
+        S = scale * qf[:, g, :] @ kf.T
+        S = np.where(causal, S, -np.inf)
+        S -= S.max(axis=1, keepdims=True)
+        Pm = np.exp(S)
+        Pm /= Pm.sum(axis=1, keepdims=True)
+        M += Pm.reshape(T, tile, T, tile).sum(axis=(1, 3))
+    return M
+
+
+def top_count(fraction: float, candidates: int) -> int:
+    """Number of candidates kept: ceil(fraction * candidates - 1e-4), each operation rounded
+    to float32 (the slack keeps exact products such as 0.25 * 8 from rounding up)."""
+    prod = np.float32(np.float32(fraction) * np.float32(candidates))
+    return int(np.ceil(np.float32(prod - np.float32(1e-4))))
+
+
+def select_top(mass: np.ndarray, kcount: int) -> np.ndarray:
+    """Indices of the kcount largest entries (ties: lower index first)."""
+    order = sorted(range(len(mass)), key=lambda j: (-mass[j], j))
+    return np.array(sorted(order[:kcount]), dtype=np.int64)
+
+
+def build_bits(layout, layer, q, k, la_fraction, ca_fraction, scale=None):
+    """LA/CA words of one layer from document-alone attention (the offline profiler):
+      LA row i keeps the top_count(la_fraction, i) tiles j < i of largest M[i][j];
+      CA keeps the top_count(ca_fraction, T) pages j of largest mean mass received from
+      the document's rows i >= j, sum_{i>=j} M[i][j] / (T - j).
+    Returns (la_words, ca_words, masses) with the layer's blocks filled (other layers 0)
+    and masses[(g, h)] = M for validation."""
+    B, Hkv = layout.tile, layout.num_kv_heads
+    G = layout.num_q_heads // Hkv
+    scale = (1.0 / np.sqrt(layout.head_dim)) if scale is None else float(scale)
+    la = np.zeros(layout.la_words_len, np.uint64)
+    ca = np.zeros(layout.ca_words_len, np.uint64)
+    masses = {}
+    for g in range(layout.num_docs):
+        s0, e0 = layout.doc_start(g), int(layout.doc_end[g])
+        T = (e0 - s0) // B
+        W = (T + 63) // 64
+        for h in range(Hkv):
+            M = doc_tile_masses(q, k, s0, e0, h, G, B, scale)
+            masses[(g, h)] = M
+            lab = np.zeros((T, W * 64), bool)
+            for i in range(1, T):
+                lab[i, select_top(M[i, :i], top_count(la_fraction, i))] = True
+            col = np.array([M[j:, j].sum() / (T - j) for j in range(T)])
+            cab = np.zeros(W * 64, bool)
+            cab[select_top(col, top_count(ca_fraction, T))] = True
+            base = layout.la_off[g] + (layer * Hkv + h) * T * W
+            la[base: base + T * W] = np.packbits(lab, axis=1, bitorder="little").view("<u8").reshape(-1)
+            cbase = layout.ca_off[g] + (layer * Hkv + h) * W
+            ca[cbase: cbase + W] = np.packbits(cab, bitorder="little").view("<u8")
+    return la, ca, masses

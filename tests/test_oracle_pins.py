@@ -303,3 +303,74 @@ def test_schedule_is_longest_first_permutation():
         assert sorted(sched[l]) == list(range(flat.shape[1]))
         c = flat[l][sched[l]]
         assert np.all(np.diff(c) <= 0)
+
+
+# ---- offline bit building (the step before the online path) -------------------------
+
+def test_build_masses_rows_sum_to_group_rows():
+    """Every query row's probabilities sum to 1, so row i of M sums to G * tile."""
+    cfg = W.custom_config("bb_rows", [([256, 512], 64)], W.BitSpec(la_p=0.3, ca_p=0.3),
+                          num_q_heads=4, num_kv_heads=2, head_dim=32, tile=64)
+    lay = W.make_layout(cfg)
+    q, k, _ = W.make_qkv(cfg, 0)
+    _, _, masses = oracle.build_bits(lay, 0, q, k, 0.3, 0.3)
+    for (g, h), M in masses.items():
+        np.testing.assert_allclose(M.sum(axis=1), 2 * 64, rtol=1e-12)
+        assert np.all(np.triu(M, 1) == 0)
+
+
+def test_build_masses_match_attention_with_one_hot_values():
+    """The tile masses equal the oracle's own attention rows when V is the one-hot tile
+    indicator of each key (document-alone problem): a second route to M."""
+    cfg = W.custom_config("bb_route", [([192, 128], 64)], W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=8, tile=64)
+    lay = W.make_layout(cfg)
+    q, k, _ = W.make_qkv(cfg, 0)
+    _, _, masses = oracle.build_bits(lay, 0, q, k, 0.5, 0.5, scale=0.2)
+    for g in range(lay.num_docs):
+        s0, e0 = lay.doc_start(g), int(lay.doc_end[g])
+        n = e0 - s0
+        sub = W.Layout(num_prompts=1, num_docs=0, num_layers=1, num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, tile=64, total_tokens=n, max_tiles_per_prompt=n // 64,
+                       cu_seqlens=np.array([0, n], np.int32), doc_cu=np.array([0, 0], np.int32),
+                       doc_end=np.zeros(0, np.int32), la_off=np.zeros(0, np.int64),
+                       ca_off=np.zeros(0, np.int64), la_words_len=0, ca_words_len=0)
+        onehot = torch.zeros((n, 1, 8))
+        onehot[torch.arange(n), 0, torch.arange(n) // 64] = 1.0
+        tok = np.repeat(np.arange(n, dtype=np.int32), 2)
+        head = np.tile(np.arange(2, dtype=np.int32), n)
+        o, _ = oracle.attention_rows(sub, np.zeros(0, np.uint64), np.zeros(0, np.uint64), 0,
+                                     q[s0:e0], k[s0:e0], onehot.to(torch.bfloat16), tok, head,
+                                     scale=0.2)
+        M2 = o.reshape(n // 64, 64, 2, 8).sum(axis=(1, 2))[:, : n // 64]
+        np.testing.assert_allclose(masses[(g, 0)], M2, atol=1e-10)
+
+
+def test_build_selects_planted_hot_tile():
+    """A key tile whose keys align with every query draws almost all the mass: LA keeps it in
+    every row below it, and it is the only page CA keeps at a one-page budget."""
+    cfg = W.custom_config("bb_hot", [([512], 64)], W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=16, tile=64)
+    lay = W.make_layout(cfg)
+    gen = torch.Generator().manual_seed(5)
+    a = torch.randn(16, generator=gen)
+    q = (a + 0.05 * torch.randn((512, 2, 16), generator=gen)).to(torch.bfloat16)
+    k = (0.05 * torch.randn((512, 1, 16), generator=gen)).to(torch.bfloat16)
+    k[2 * 64: 3 * 64, 0] = (2.0 * a).to(torch.bfloat16)          # tile 2 is hot
+    la, ca, _ = oracle.build_bits(lay, 0, q, k, 1.0 / 8, 1.0 / 8, scale=1.0)
+    for i in range(3, 8):  # rows below the hot tile keep exactly one LA tile (ceil(i/8) = 1)
+        assert int(la[i]) == 1 << 2, (i, bin(int(la[i])))
+    assert int(ca[0]) == 1 << 2
+
+
+def test_build_counts_follow_the_fractions():
+    cfg = W.custom_config("bb_cnt", [([64 * 20, 64 * 7], 64)], W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=16, tile=64)
+    lay = W.make_layout(cfg)
+    q, k, _ = W.make_qkv(cfg, 0)
+    la, ca, _ = oracle.build_bits(lay, 0, q, k, 0.25, 0.4)
+    for g, T in ((0, 20), (1, 7)):
+        base = lay.la_off[g]
+        for i in range(T):
+            assert bin(int(la[base + i])).count("1") == int(np.ceil(0.25 * i - 1e-4))
+        assert bin(int(ca[lay.ca_off[g]])).count("1") == int(np.ceil(0.4 * T - 1e-4))
