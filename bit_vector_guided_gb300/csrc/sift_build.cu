@@ -81,20 +81,24 @@ __global__ void segments_kernel(const int32_t *cu, const int32_t *doc_cu, const 
     for (int k = 0; k <= P + D; ++k) seg_doc_cu[k] = 0;
 }
 
-// V[u][h][c] = 1 where c is the tile of u inside its segment minus the window start
+// V[u][h][c] = 1 where c is the tile of u inside its segment minus the window start; one
+// thread per 8 columns (one 16-byte store), consecutive threads on consecutive bytes
 __global__ void onehot_kernel(const int32_t *seg_cu, int S, int T, int Hkv, int d, int B,
-                              int window, __nv_bfloat16 *v) {
-    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (u, h)
-    if (e >= static_cast<int64_t>(T) * Hkv) return;
-    const int u = static_cast<int>(e / Hkv);
+                              int window, uint4 *v) {
+    const int chunks = d / 8;
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= static_cast<int64_t>(T) * Hkv * chunks) return;
+    const int u = static_cast<int>(e / (static_cast<int64_t>(Hkv) * chunks));
+    const int c0 = static_cast<int>(e % chunks) * 8;
     int lo = 0, hi = S - 1;  // segment of u: last s with seg_cu[s] <= u
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (__ldg(seg_cu + mid) <= u) lo = mid; else hi = mid - 1;
     }
-    const int col = (u - __ldg(seg_cu + lo)) / B - window * d;
-    __nv_bfloat16 *row = v + e * d;
-    for (int c = 0; c < d; ++c) row[c] = __float2bfloat16(c == col ? 1.f : 0.f);
+    const int k = (u - __ldg(seg_cu + lo)) / B - window * d - c0;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (k >= 0 && k < 8) w[k >> 1] = (k & 1) ? 0x3f800000u : 0x00003f80u;  // bf16 1.0
+    v[e] = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 struct DocGeom {
@@ -114,35 +118,49 @@ __device__ __forceinline__ DocGeom doc_geom(const int32_t *cu, const int32_t *do
 }
 
 // M[g][h][i][j] for the key tiles j of this window: sum over the group's query heads and
-// the rows of query tile i of O[t][qh][j - window*d], in a fixed order
-__global__ void mass_kernel(const __nv_bfloat16 *o, const int32_t *cu, const int32_t *doc_cu,
-                            const int32_t *doc_end, int P, int B, int Hq, int Hkv, int d,
-                            int maxT, int window, int total_tokens, float *mass) {
+// the rows of query tile i of O[t][qh][j - window*d].  One 256-thread block per (document,
+// kv head, query tile): warp w sums rows w, w+8, ... (lane = 4 columns, one 8-byte load
+// per row), then the 8 partial sums are added in warp order -- a fixed order.
+constexpr int kMassWarps = 8;
+
+__global__ void __launch_bounds__(32 * kMassWarps)
+mass_kernel(const __nv_bfloat16 *o, const int32_t *cu, const int32_t *doc_cu,
+            const int32_t *doc_end, int P, int B, int Hq, int Hkv, int d, int maxT, int window,
+            int total_tokens, float *mass) {
+    __shared__ float part[kMassWarps][128];
     const int g = blockIdx.y;
-    const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    const int h = wid / maxT, i = wid % maxT;
-    if (h >= Hkv) return;
+    const int h = blockIdx.x / maxT, i = blockIdx.x % maxT;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DocGeom dg = doc_geom(cu, doc_cu, doc_end, P, g, B);
-    if (i >= dg.tiles || dg.tiles > maxT || dg.start < 0 ||
+    if (h >= Hkv || i >= dg.tiles || dg.tiles > maxT || dg.start < 0 ||
         static_cast<int64_t>(dg.start) + static_cast<int64_t>(dg.tiles) * B > total_tokens)
-        return;  // malformed documents are reported by the segments kernel
+        return;  // block-uniform; malformed documents are reported by the segments kernel
     const int G = Hq / Hkv;
-    const int j0 = window * d;
+    const int c = 4 * lane;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int qh = h * G; qh < (h + 1) * G; ++qh)
-        for (int r = 0; r < B; ++r) {
-            const int64_t t = static_cast<int64_t>(dg.start) + static_cast<int64_t>(i) * B + r;
-            const __nv_bfloat16 *row = o + (t * Hq + qh) * d;
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const int c = lane + 32 * q4;
-                if (c < d) acc[q4] += __bfloat162float(row[c]);
-            }
+    if (c < d) {
+        const int64_t t0 = static_cast<int64_t>(dg.start) + static_cast<int64_t>(i) * B;
+#pragma unroll 4
+        for (int rr = warp; rr < G * B; rr += kMassWarps) {
+            const int qh = h * G + rr / B;
+            const int64_t t = t0 + rr % B;
+            const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(o + (t * Hq + qh) * d + c));
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+            acc[0] += a.x;
+            acc[1] += a.y;
+            acc[2] += b.x;
+            acc[3] += b.y;
         }
-    float *out = mass + ((static_cast<int64_t>(g) * Hkv + h) * maxT + i) * maxT;
-    for (int q4 = 0; q4 < 4; ++q4) {
-        const int j = j0 + lane + 32 * q4;
-        if (lane + 32 * q4 < d && j <= i && j < dg.tiles) out[j] = acc[q4];
+        for (int q = 0; q < 4; ++q) part[warp][c + q] = acc[q];
+    }
+    __syncthreads();
+    if (threadIdx.x < d) {
+        float sum = 0.f;
+        for (int w = 0; w < kMassWarps; ++w) sum += part[w][threadIdx.x];
+        const int j = window * d + static_cast<int>(threadIdx.x);
+        if (j <= i && j < dg.tiles)
+            mass[((static_cast<int64_t>(g) * Hkv + h) * maxT + i) * maxT + j] = sum;
     }
 }
 
@@ -286,16 +304,15 @@ extern "C" sift_status sift_build_bits(const sift_problem *prob, int32_t layer, 
     seg.ca_words_len = 0;
     const int windows = (max_doc_tiles + d - 1) / d;
     for (int w = 0; w < windows; ++w) {
-        const int64_t n = static_cast<int64_t>(T) * Hkv;
+        const int64_t n = static_cast<int64_t>(T) * Hkv * (d / 8);
         onehot_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(
-            seg_cu, bl.segments, T, Hkv, d, B, w, v1);
+            seg_cu, bl.segments, T, Hkv, d, B, w, reinterpret_cast<uint4 *>(v1));
         if (cudaGetLastError() != cudaSuccess) return SIFT_ERR_CUDA;
         st = sift_dense_prefill(&seg, q, k, v1, softmax_scale, o, lse, dws, dws_bytes, dev_status,
                                 stream);
         if (st != SIFT_OK) return st;
-        const int warps = Hkv * max_doc_tiles;
-        dim3 grid(static_cast<unsigned>((warps + 7) / 8), static_cast<unsigned>(D));
-        mass_kernel<<<grid, 256, 0, stream>>>(o, prob->cu_seqlens, prob->doc_cu, prob->doc_end,
+        dim3 grid(static_cast<unsigned>(Hkv * max_doc_tiles), static_cast<unsigned>(D));
+        mass_kernel<<<grid, 32 * kMassWarps, 0, stream>>>(o, prob->cu_seqlens, prob->doc_cu, prob->doc_end,
                                               prob->num_prompts, B, Hq, Hkv, d, max_doc_tiles, w,
                                               T, mass);
         if (cudaGetLastError() != cudaSuccess) return SIFT_ERR_CUDA;
