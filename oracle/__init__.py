@@ -36,7 +36,8 @@ _LIB = os.path.join(_HERE, "_build", "libsift_oracle.so")
 _lib = None
 
 __all__ = ["build", "load", "decode", "schedule", "attention_rows", "attention_all",
-           "key_mask", "brute_force_attention", "tile_mask", "set_threads",
+           "key_mask", "brute_force_attention", "tile_mask", "set_threads", "decode_ragged",
+           "token_mask",
            "doc_tile_masses", "top_count", "select_top", "build_bits"]
 
 
@@ -64,11 +65,14 @@ def load():
         i32, i64, f64 = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
         lib.sift_oracle_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, P, P]
         lib.sift_oracle_decode.restype = i32
-        lib.sift_oracle_attention_rows.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32,
-                                                   i32, i32, f64, P, P, P, i64, P, P, P, P]
+        lib.sift_oracle_decode_ragged.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P,
+                                                  P, P, i32, i32, P, P, P]
+        lib.sift_oracle_decode_ragged.restype = i32
+        lib.sift_oracle_attention_rows.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
+                                                   i32, i32, i32, f64, P, P, P, i64, P, P, P, P]
         lib.sift_oracle_attention_rows.restype = i32
-        lib.sift_oracle_key_mask.argtypes = [i32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
-                                             i64, P, i64, P, P]
+        lib.sift_oracle_key_mask.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32,
+                                             i32, i64, P, i64, P, P]
         lib.sift_oracle_key_mask.restype = i32
         lib.sift_oracle_set_threads.argtypes = [i32]
         lib.sift_oracle_set_threads.restype = i32
@@ -100,8 +104,14 @@ def _layout_args(layout, la_words, ca_words):
     return arrs
 
 
+def _page(layout) -> int:
+    page = int(getattr(layout, "page", 0) or 0)
+    return page if page > 0 else int(layout.tile)
+
+
 def decode(layout, la_words, ca_words, rowcap: Optional[int] = None):
-    """Tile index lists of every (layer, kv head, query tile) row.
+    """Tile index lists of every (layer, kv head, query tile) row (aligned layouts:
+    page == tile and every boundary a multiple of the tile).
 
     Returns (kv_idx int32 [L, Hkv, N, rowcap] with -1 padding, counts int32 [L, Hkv, N]).
     """
@@ -116,6 +126,28 @@ def decode(layout, la_words, ca_words, rowcap: Optional[int] = None):
     if rc != 0:
         raise ValueError("oracle decode: a row exceeds rowcap")
     return kv_idx, counts
+
+
+def decode_ragged(layout, la_words, ca_words, rowcap: Optional[int] = None):
+    """Per-segment query tiles and their (first token, info) key-tile lists, for documents
+    of any length and a CA page size of its own (rule in sift_oracle.c).
+
+    Returns (qtiles int32 [NQ, 2], kv int32 [L, Hkv, NQ, rowcap, 2] with -1 padding,
+    counts int32 [L, Hkv, NQ]).
+    """
+    lib = load()
+    rowcap = rowcap or layout.max_tiles_per_prompt
+    L, Hkv, NQ = layout.num_layers, layout.num_kv_heads, layout.num_query_tiles
+    qtiles = np.zeros((max(NQ, 1), 2), np.int32)
+    kv = np.full((L, Hkv, max(NQ, 1), rowcap, 2), -1, np.int32)
+    counts = np.zeros((L, Hkv, max(NQ, 1)), np.int32)
+    arrs = _layout_args(layout, la_words, ca_words)
+    rc = lib.sift_oracle_decode_ragged(layout.num_prompts, layout.num_docs, L, Hkv, layout.tile,
+                                       _page(layout), *[_ptr(a) for a in arrs], NQ, rowcap,
+                                       _ptr(qtiles), _ptr(kv), _ptr(counts))
+    if rc != 0:
+        raise ValueError("oracle ragged decode: bad page size, tile count or row capacity")
+    return qtiles[:NQ], kv[:, :, :NQ], counts[:, :, :NQ]
 
 
 def schedule(counts: np.ndarray) -> np.ndarray:
@@ -153,7 +185,7 @@ def attention_rows(layout, la_words, ca_words, layer, q, k, v, row_tok, row_head
     out_lse = np.zeros(max(n, 1), np.float64)
     arrs = _layout_args(layout, la_words, ca_words)
     rc = lib.sift_oracle_attention_rows(
-        layout.num_prompts, layout.num_docs, layout.num_kv_heads, layout.tile,
+        layout.num_prompts, layout.num_docs, layout.num_kv_heads, layout.tile, _page(layout),
         *[_ptr(a) for a in arrs], int(layer), layout.num_q_heads, d, scale,
         _ptr(qb), _ptr(kb), _ptr(vb), n, _ptr(row_tok), _ptr(row_head),
         _ptr(out_o), _ptr(out_lse))
@@ -179,7 +211,8 @@ def key_mask(layout, la_words, ca_words, layer, kv_head, q_tok, k_tok) -> np.nda
     out = np.zeros((len(q_tok), len(k_tok)), np.uint8)
     arrs = _layout_args(layout, la_words, ca_words)
     lib.sift_oracle_key_mask(layout.num_prompts, layout.num_docs, layout.num_kv_heads,
-                             layout.tile, *[_ptr(a) for a in arrs], int(layer), int(kv_head),
+                             layout.tile, _page(layout), *[_ptr(a) for a in arrs], int(layer),
+                             int(kv_head),
                              len(q_tok), _ptr(q_tok), len(k_tok), _ptr(k_tok), _ptr(out))
     return out.astype(bool)
 
@@ -231,8 +264,46 @@ def tile_mask(layout, la_words, ca_words, layer, kv_head) -> np.ndarray:
     return M
 
 
+def token_mask(layout, la_words, ca_words, layer, kv_head) -> np.ndarray:
+    """Token-level mask M[t, u] (query token t may use key token u), any layout.
+
+    Built block by block from the plain description, with tiles and pages counted
+    from each document's first token: a document's block holds its own LA tiles
+    (plus every token's own tile), a later document's block against an earlier one
+    holds the earlier one's CA-flagged pages, the query suffix sees its whole prompt,
+    and everything is causal.
+    """
+    B, Pg, Hkv = layout.tile, _page(layout), layout.num_kv_heads
+    T = layout.total_tokens
+    M = np.zeros((T, T), bool)
+    for p in range(layout.num_prompts):
+        c0, c1 = int(layout.cu_seqlens[p]), int(layout.cu_seqlens[p + 1])
+        earlier = []
+        last = c0
+        for g in range(int(layout.doc_cu[p]), int(layout.doc_cu[p + 1])):
+            s0, e0 = layout.doc_start(g), int(layout.doc_end[g])
+            n = e0 - s0
+            Tg, Cg = -(-n // B), -(-n // Pg)
+            W, V = -(-Tg // 64), -(-Cg // 64)
+            base = int(layout.la_off[g]) + (layer * Hkv + kv_head) * Tg * W
+            la = _unpack(np.asarray(la_words[base: base + Tg * W]).reshape(Tg, W), Tg)
+            cbase = int(layout.ca_off[g]) + (layer * Hkv + kv_head) * V
+            ca = _unpack(np.asarray(ca_words[cbase: cbase + V]).reshape(1, V), Cg)[0]
+            tl = np.arange(n) // B
+            same = tl[:, None] == tl[None, :]
+            below = la[tl[:, None], tl[None, :]] & (tl[None, :] < tl[:, None])
+            M[s0:e0, s0:e0] = same | below
+            for (s2, e2, keep2) in earlier:
+                M[s0:e0, s2:e2] = keep2[None, :]
+            earlier.append((s0, e0, ca[np.arange(n) // Pg]))
+            last = e0
+        M[last:c1, c0:c1] = True
+    return M & np.tril(np.ones((T, T), bool))
+
+
 def brute_force_attention(layout, la_words, ca_words, layer, q, k, v, scale=None):
-    """Dense fp64 attention with -inf outside the expanded token mask (tiny inputs only)."""
+    """Dense fp64 attention with -inf outside the token mask (tiny inputs only): the tile
+    mask expanded to tokens for aligned layouts, token_mask otherwise."""
     qb = _bf16_bits(q).astype(np.uint32) << 16
     kb = _bf16_bits(k).astype(np.uint32) << 16
     vb = _bf16_bits(v).astype(np.uint32) << 16
@@ -247,9 +318,13 @@ def brute_force_attention(layout, la_words, ca_words, layer, q, k, v, scale=None
     causal = np.tril(np.ones((T, T), bool))
     O = np.zeros((T, Hq, d))
     LSE = np.zeros((Hq, T))
+    aligned = getattr(layout, "aligned", True)
     for h in range(Hkv):
-        M = np.kron(tile_mask(layout, la_words, ca_words, layer, h),
-                    np.ones((B, B), bool)) & causal
+        if aligned:
+            M = np.kron(tile_mask(layout, la_words, ca_words, layer, h),
+                        np.ones((B, B), bool)) & causal
+        else:
+            M = token_mask(layout, la_words, ca_words, layer, h)
         for qh in range(h * G, (h + 1) * G):
             S = scale * qf[:, qh, :] @ kf[:, h, :].T
             S = np.where(M, S, -np.inf)

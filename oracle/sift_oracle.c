@@ -27,11 +27,17 @@
  * ascending order.  Rows are independent, so OpenMP over rows changes no
  * result.
  *
- * Parity pins (checked by the "not gpu" tests): a hand-derived decode fixture,
- * popcount identities, all-ones bits == dense causal attention (library SDPA),
- * per-document / block-diagonal / cross-document special cases against SDPA
- * with a mask built from their plain description, closed forms (first token,
- * constant V), and a dense-mask brute force on tiny inputs.
+ * Documents of any length and a CA page size that differs from the tile
+ * (the pages fix neither) follow one reading: tiles and pages are counted
+ * from each document's first token, the last ones partial (key_visible and
+ * sift_oracle_decode_ragged below).
+ *
+ * Parity pins (checked by the "not gpu" tests): hand-derived decode fixtures
+ * (aligned and ragged), popcount identities, all-ones bits == dense causal
+ * attention (library SDPA), per-document / block-diagonal / cross-document
+ * special cases against SDPA with a mask built from their plain description,
+ * closed forms (first token, constant V), single planted CA bits against their
+ * page's token range, and dense-mask numpy brute forces on tiny inputs.
  */
 #include <math.h>
 #include <stdint.h>
@@ -43,6 +49,7 @@
 
 typedef struct {
     int num_prompts, num_docs, num_kv_heads, tile;
+    int page;                  /* CA page size in tokens (equal to tile unless stated) */
     const int32_t *cu_seqlens; /* [P+1] token offsets of each prompt          */
     const int32_t *doc_cu;     /* [P+1] prompt p owns docs doc_cu[p]..[p+1]-1 */
     const int32_t *doc_end;    /* [D] absolute end token (exclusive)          */
@@ -70,8 +77,16 @@ static int doc_of(const sift_bits_view *s, int p, int64_t t) {
     return -1;
 }
 
+/* LA tiles of document g, counted from its first token; the last may be partial */
 static int doc_tiles(const sift_bits_view *s, int p, int g) {
-    return (int)((s->doc_end[g] - doc_begin(s, p, g)) / s->tile);
+    int64_t n = s->doc_end[g] - doc_begin(s, p, g);
+    return (int)((n + s->tile - 1) / s->tile);
+}
+
+/* CA pages of document g, counted from its first token; the last may be partial */
+static int doc_pages(const sift_bits_view *s, int p, int g) {
+    int64_t n = s->doc_end[g] - doc_begin(s, p, g);
+    return (int)((n + s->page - 1) / s->page);
 }
 
 /* LA bit (row i, column j) of document g for (layer, kv head h).
@@ -85,10 +100,11 @@ static int la_bit(const sift_bits_view *s, int p, int g, int layer, int h, int i
     return (int)((word >> (j % 64)) & 1u);
 }
 
-/* CA bit of page j of document g for (layer, kv head h); same bit order as LA. */
+/* CA bit of page j of document g for (layer, kv head h); same bit order as LA,
+ * ceil(C/64) words for the document's C pages. */
 static int ca_bit(const sift_bits_view *s, int p, int g, int layer, int h, int j) {
-    int T = doc_tiles(s, p, g);
-    int W = (T + 63) / 64;
+    int C = doc_pages(s, p, g);
+    int W = (C + 63) / 64;
     int64_t base = s->ca_off[g] + ((int64_t)layer * s->num_kv_heads + h) * W;
     uint64_t word = s->ca_words[base + j / 64];
     return (int)((word >> (j % 64)) & 1u);
@@ -99,11 +115,17 @@ static int ca_bit(const sift_bits_view *s, int p, int g, int layer, int h, int j
  *   - keys come from t's own prompt and are causal (u <= t);
  *   - a query in the user suffix attends to every earlier key of the prompt
  *     (no metadata exists for the fresh query);
- *   - the diagonal tile (key tile == query tile) is always computed;
+ *   - tiles and pages are counted from the first token of their document:
+ *     token x of document g lies in tile (x - start_g) / tile and in page
+ *     (x - start_g) / page;
+ *   - the diagonal tile (key tile == query tile of the same document) is
+ *     always computed;
  *   - a key in t's own document g: its tile column j is kept iff LA[g][i][j];
  *   - a key in an earlier document g' of the prompt: its page is kept iff
  *     CA[g'][page];
  *   - everything else is skipped.
+ * With every boundary a multiple of the tile and page == tile, document tiles
+ * coincide with the global tiles token / tile.
  */
 static int key_visible(const sift_bits_view *s, int layer, int h, int64_t t, int64_t u) {
     int p = prompt_of(s, t);
@@ -111,14 +133,14 @@ static int key_visible(const sift_bits_view *s, int layer, int h, int64_t t, int
     int g = doc_of(s, p, t);
     if (g < 0) return 1;
     int64_t B = s->tile;
-    if (t / B == u / B) return 1;
     int gu = doc_of(s, p, u);
     if (gu == g) {
         int64_t d0 = doc_begin(s, p, g);
+        if ((t - d0) / B == (u - d0) / B) return 1;
         return la_bit(s, p, g, layer, h, (int)((t - d0) / B), (int)((u - d0) / B));
     }
     int64_t d0u = doc_begin(s, p, gu);
-    return ca_bit(s, p, gu, layer, h, (int)((u - d0u) / B));
+    return ca_bit(s, p, gu, layer, h, (int)((u - d0u) / s->page));
 }
 
 /*
@@ -136,7 +158,7 @@ int sift_oracle_decode(int num_prompts, int num_docs, int num_layers, int num_kv
                        const int64_t *la_off, const int64_t *ca_off,
                        const uint64_t *la_words, const uint64_t *ca_words,
                        int rowcap, int32_t *kv_idx, int32_t *counts) {
-    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, cu_seqlens, doc_cu,
+    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, tile, cu_seqlens, doc_cu,
                         doc_end, la_off, ca_off, la_words, ca_words};
     int64_t N = cu_seqlens[num_prompts] / tile;
     int bad = 0;
@@ -170,6 +192,106 @@ int sift_oracle_decode(int num_prompts, int num_docs, int num_layers, int num_kv
     return bad ? -1 : 0;
 }
 
+/*
+ * Decode for documents of any length and a CA page size of its own.
+ *
+ * Query tiles: every segment -- a document, or a prompt's query suffix -- is
+ * cut into tiles of `tile` tokens from its own first token, the last one
+ * possibly partial.  Tiles are numbered q = 0, 1, ... in token order and
+ * qtiles[2q], qtiles[2q+1] = (first token, rows).  Key tiles are cut the
+ * same way.
+ *
+ * Row (l, h, q) lists key tiles as pairs (first token, info), by ascending
+ * first token:
+ *   - a document row: every tile of each earlier document of the prompt
+ *     that holds a CA-flagged page, then the LA-flagged tiles j < i of the
+ *     row's own document, then the diagonal tile;
+ *   - a suffix row: every tile of every document of the prompt, the suffix's
+ *     own tiles before the diagonal, then the diagonal.
+ * info = len | causal << 8 | mask << 16, with Pin = min(page, tile):
+ *   len     keys of the tile inside its segment (1 .. tile);
+ *   causal  1 on the diagonal only;
+ *   mask    bit k covers keys [k*Pin, (k+1)*Pin) of the tile; all tile/Pin
+ *           bits for every tile but a CA one, whose bit k is the CA bit of
+ *           the page holding key k*Pin (0 when k*Pin >= len).
+ * Key (first + c) of an entry is visible to row r of the query tile iff
+ * c < len, mask bit c / Pin is set, and c <= r when causal -- the same key
+ * set as key_visible().  kv holds rowcap pairs per row, row (l*Hkv + h)*nq + q.
+ * Returns 0, or -1 if the segments do not make nq tiles or a row exceeds rowcap.
+ */
+int sift_oracle_decode_ragged(int num_prompts, int num_docs, int num_layers, int num_kv_heads,
+                              int tile, int page, const int32_t *cu_seqlens,
+                              const int32_t *doc_cu, const int32_t *doc_end,
+                              const int64_t *la_off, const int64_t *ca_off,
+                              const uint64_t *la_words, const uint64_t *ca_words, int nq,
+                              int rowcap, int32_t *qtiles, int32_t *kv, int32_t *counts) {
+    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, page, cu_seqlens, doc_cu,
+                        doc_end, la_off, ca_off, la_words, ca_words};
+    if (tile < 1 || page < 1 || (page < tile ? tile % page : page % tile) != 0 ||
+        tile / (page < tile ? page : tile) > 16)
+        return -1;  /* pages must nest with tiles, at most 16 pages per tile */
+    const int pin = page < tile ? page : tile;
+    const int nbits = tile / pin;
+    const uint32_t full = (1u << nbits) - 1u;
+    int bad = 0;
+    int q = 0;
+    for (int p = 0; p < num_prompts; ++p)
+        for (int g = doc_cu[p]; g <= doc_cu[p + 1]; ++g) {  /* g == doc_cu[p+1]: the suffix */
+            int64_t start = g < doc_cu[p + 1] ? doc_begin(&s, p, g)
+                            : (doc_cu[p + 1] > doc_cu[p] ? doc_end[doc_cu[p + 1] - 1]
+                                                         : cu_seqlens[p]);
+            int64_t end = g < doc_cu[p + 1] ? doc_end[g] : cu_seqlens[p + 1];
+            for (int64_t x = start; x < end; x += tile, ++q)
+                if (q < nq) {
+                    qtiles[2 * q] = (int32_t)x;
+                    qtiles[2 * q + 1] = (int32_t)(end - x < tile ? end - x : tile);
+                }
+        }
+    if (q != nq) return -1;
+    for (int l = 0; l < num_layers; ++l)
+        for (int h = 0; h < num_kv_heads; ++h) {
+            q = 0;
+            for (int p = 0; p < num_prompts; ++p)
+                for (int g = doc_cu[p]; g <= doc_cu[p + 1]; ++g) {
+                    int suffix = g == doc_cu[p + 1];
+                    int64_t start = !suffix ? doc_begin(&s, p, g)
+                                    : (doc_cu[p + 1] > doc_cu[p] ? doc_end[doc_cu[p + 1] - 1]
+                                                                 : cu_seqlens[p]);
+                    int64_t end = !suffix ? doc_end[g] : cu_seqlens[p + 1];
+                    for (int64_t x = start; x < end; x += tile, ++q) {
+                        int64_t row = ((int64_t)l * num_kv_heads + h) * nq + q;
+                        int32_t *out = kv + row * rowcap * 2;
+                        int n = 0;
+#define EMIT(first, info) do { if (n < rowcap) { out[2 * n] = (int32_t)(first); \
+                               out[2 * n + 1] = (int32_t)(info); } else bad = 1; ++n; } while (0)
+                        for (int gp = doc_cu[p]; gp < g; ++gp) {
+                            int64_t ds = doc_begin(&s, p, gp), de = doc_end[gp];
+                            for (int64_t y = ds; y < de; y += tile) {
+                                int64_t len = de - y < tile ? de - y : tile;
+                                uint32_t mask = 0;
+                                if (suffix) {
+                                    mask = full;
+                                } else {
+                                    for (int k = 0; k < nbits && (int64_t)k * pin < len; ++k)
+                                        if (ca_bit(&s, p, gp, l, h, (int)((y - ds + (int64_t)k * pin) / page)))
+                                            mask |= 1u << k;
+                                }
+                                if (mask) EMIT(y, (uint32_t)len | mask << 16);
+                            }
+                        }
+                        int64_t i = (x - start) / tile;
+                        for (int64_t j = 0; j < i; ++j)
+                            if (suffix || la_bit(&s, p, g, l, h, (int)i, (int)j))
+                                EMIT(start + j * tile, (uint32_t)tile | full << 16);
+                        EMIT(x, (uint32_t)(end - x < tile ? end - x : tile) | 1u << 8 | full << 16);
+#undef EMIT
+                        counts[row] = n;
+                    }
+                }
+        }
+    return bad ? -1 : 0;
+}
+
 static double bf16_to_double(uint16_t x) {
     uint32_t b = (uint32_t)x << 16;
     float f;
@@ -189,7 +311,7 @@ static double bf16_to_double(uint16_t x) {
  * Returns 0, or -1 on a row outside the batch.
  */
 int sift_oracle_attention_rows(int num_prompts, int num_docs, int num_kv_heads, int tile,
-                               const int32_t *cu_seqlens, const int32_t *doc_cu,
+                               int page, const int32_t *cu_seqlens, const int32_t *doc_cu,
                                const int32_t *doc_end, const int64_t *la_off,
                                const int64_t *ca_off, const uint64_t *la_words,
                                const uint64_t *ca_words, int layer, int num_q_heads,
@@ -197,7 +319,7 @@ int sift_oracle_attention_rows(int num_prompts, int num_docs, int num_kv_heads, 
                                const uint16_t *k, const uint16_t *v, int64_t nrows,
                                const int32_t *row_tok, const int32_t *row_head,
                                double *out_o, double *out_lse) {
-    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, cu_seqlens, doc_cu,
+    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, page, cu_seqlens, doc_cu,
                         doc_end, la_off, ca_off, la_words, ca_words};
     const int G = num_q_heads / num_kv_heads;
     const int d = head_dim;
@@ -246,12 +368,12 @@ int sift_oracle_attention_rows(int num_prompts, int num_docs, int num_kv_heads, 
 
 /* Same key-set definition, exposed for the cross-check against the decoded lists:
  * writes a [nq][nk] 0/1 matrix for query tokens q_tok and key tokens k_tok. */
-int sift_oracle_key_mask(int num_prompts, int num_docs, int num_kv_heads, int tile,
+int sift_oracle_key_mask(int num_prompts, int num_docs, int num_kv_heads, int tile, int page,
                          const int32_t *cu_seqlens, const int32_t *doc_cu, const int32_t *doc_end,
                          const int64_t *la_off, const int64_t *ca_off, const uint64_t *la_words,
                          const uint64_t *ca_words, int layer, int kv_head, int64_t nq,
                          const int32_t *q_tok, int64_t nk, const int32_t *k_tok, uint8_t *out) {
-    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, cu_seqlens, doc_cu,
+    sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, page, cu_seqlens, doc_cu,
                         doc_end, la_off, ca_off, la_words, ca_words};
     for (int64_t a = 0; a < nq; ++a)
         for (int64_t b = 0; b < nk; ++b)

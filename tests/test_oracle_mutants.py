@@ -2,8 +2,9 @@
 
 Each case copies oracle/sift_oracle.c, plants one mistake by a text substitution,
 builds the copy with gcc in a temporary directory and runs the unchanged pins of
-tests/test_oracle_pins.py against it (SIFT_ORACLE_LIB points the oracle at the
-copy).  Every mutant must make at least one pin fail.
+tests/test_oracle_pins.py and tests/test_oracle_ragged_pins.py against it
+(SIFT_ORACLE_LIB points the oracle at the copy).  Every mutant must make at least
+one pin fail.
 """
 import os
 import subprocess
@@ -22,7 +23,7 @@ MUTANTS = [
     ("ca_inside_own_doc",
      "return la_bit(s, p, g, layer, h, (int)((t - d0) / B), (int)((u - d0) / B));",
      "return ca_bit(s, p, g, layer, h, (int)((u - d0) / B));"),
-    ("no_diagonal", "if (t / B == u / B) return 1;", "if (0) return 1;"),
+    ("no_diagonal", "if ((t - d0) / B == (u - d0) / B) return 1;", "if (0) return 1;"),
     ("suffix_not_dense", "if (g < 0) return 1;\n    int64_t B", "if (g < 0) return 0;\n    int64_t B"),
     ("msb_first_bits", "uint64_t word = s->la_words[base + (int64_t)i * W + j / 64];\n    return (int)((word >> (j % 64)) & 1u);",
      "uint64_t word = s->la_words[base + (int64_t)i * W + j / 64];\n    return (int)((word >> (63 - j % 64)) & 1u);"),
@@ -42,6 +43,21 @@ MUTANTS = [
      "const uint16_t *vr = v + (u * num_kv_heads + (qh % num_kv_heads)) * d;"),
     ("prompt_boundary_ignored", "if (p < 0 || u < s->cu_seqlens[p] || u > t) return 0;",
      "if (p < 0 || u < 0 || u > t) return 0;"),
+    # documents of any length and a page size of its own
+    ("ca_page_is_tile", "return ca_bit(s, p, gu, layer, h, (int)((u - d0u) / s->page));",
+     "return ca_bit(s, p, gu, layer, h, (int)((u - d0u) / s->tile));"),
+    ("tiles_rounded_down", "return (int)((n + s->tile - 1) / s->tile);",
+     "return (int)(n / s->tile);"),
+    ("pages_rounded_down", "return (int)((n + s->page - 1) / s->page);",
+     "return (int)(n / s->page);"),
+    ("ragged_mask_first_page_only",
+     "if (ca_bit(&s, p, gp, l, h, (int)((y - ds + (int64_t)k * pin) / page)))",
+     "if (ca_bit(&s, p, gp, l, h, (int)((y - ds) / page)))"),
+    ("ragged_full_length_tiles", "int64_t len = de - y < tile ? de - y : tile;",
+     "int64_t len = tile;"),
+    ("ragged_diagonal_not_causal",
+     "EMIT(x, (uint32_t)(end - x < tile ? end - x : tile) | 1u << 8 | full << 16);",
+     "EMIT(x, (uint32_t)(end - x < tile ? end - x : tile) | full << 16);"),
 ]
 
 
@@ -56,6 +72,7 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
                     str(lib), "-lm"], check=True)
     env = dict(os.environ, SIFT_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_ragged_pins.py")],
                        env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -1,0 +1,279 @@
+"""Pins for the oracle's general layout: documents of any length (tiles and pages
+counted from each document's first token, the last ones partial) and a CA page size
+that differs from the LA tile.
+
+* a hand-derived ragged decode fixture (tests/golden/decode_ragged_small.json);
+* three routes to one key set: the decoded (first token, info) lists expanded to
+  tokens, the C key_visible() rule, and a block-wise numpy token mask;
+* the aligned layout as a special case of the ragged decode;
+* page-size semantics on single planted CA bits;
+* attention: special cases against torch SDPA (fp64) with masks written from the
+  plain description, and the numpy dense-mask brute force.
+
+SIFT pages: gist.science/it/paper/2606.09441, "Design del Sistema" (LA flags tiles
+of a document's own attention matrix, CA flags KV pages that later documents
+attend to) and "Dettagli di Implementazione" (bits decoded into tile indices).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden():
+    with open(os.path.join(GOLDEN, "decode_ragged_small.json")) as f:
+        g = json.load(f)
+    lay = W.Layout(num_prompts=2, num_docs=3, num_layers=g["num_layers"], num_q_heads=2,
+                   num_kv_heads=g["num_kv_heads"], head_dim=8, tile=g["tile"],
+                   total_tokens=g["cu_seqlens"][-1], max_tiles_per_prompt=6,
+                   cu_seqlens=np.array(g["cu_seqlens"], np.int32),
+                   doc_cu=np.array(g["doc_cu"], np.int32),
+                   doc_end=np.array(g["doc_end"], np.int32),
+                   la_off=np.array(g["la_off"], np.int64), ca_off=np.array(g["ca_off"], np.int64),
+                   la_words_len=len(g["la_words"]), ca_words_len=len(g["ca_words"]),
+                   page=g["page"])
+    return g, lay, np.array(g["la_words"], np.uint64), np.array(g["ca_words"], np.uint64)
+
+
+def expand_lists(lay, qtiles, kv, counts, layer, h):
+    """Token mask implied by the decoded lists: key (first + c) is visible to row r of
+    the query tile iff c < len, mask bit c // Pin is set and, when causal, c <= r."""
+    T, B = lay.total_tokens, lay.tile
+    pin = min(lay.page_size, B)
+    M = np.zeros((T, T), bool)
+    c = np.arange(B)
+    for q, (x, rows) in enumerate(qtiles):
+        r = np.arange(rows)
+        for e in range(counts[layer, h, q]):
+            first, info = (int(v) for v in kv[layer, h, q, e])
+            ln, causal, mask = info & 0xFF, (info >> 8) & 1, (info >> 16) & 0xFFFF
+            col = (c < ln) & (((mask >> (c // pin)) & 1) == 1)
+            vis = np.broadcast_to(col[None, :], (rows, B)).copy()
+            if causal:
+                vis &= c[None, :] <= r[:, None]
+            rr, cc = np.nonzero(vis)
+            M[x + rr, first + cc] = True
+    return M
+
+
+def test_ragged_golden_fixture():
+    g, lay, la, ca = _golden()
+    qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
+    assert qt.tolist() == g["expected_qtiles"]
+    for q, row in enumerate(g["expected_rows"]):
+        assert cnt[0, 0, q] == len(row), q
+        assert kv[0, 0, q, :len(row)].tolist() == row, q
+    # and the fixture's lists are the key set of the token rule
+    T = lay.total_tokens
+    tok = np.arange(T)
+    assert np.array_equal(expand_lists(lay, qt, kv, cnt, 0, 0),
+                          oracle.key_mask(lay, la, ca, 0, 0, tok, tok))
+
+
+RAGGED_CFGS = [
+    # tile 16, page 8 (2 pages per tile); odd documents, odd suffix, empty suffix,
+    # a suffix-only prompt
+    W.custom_config("rg_p8", [([6 * 16 + 5, 16 * 3, 7], 9), ([33], 0), ([], 21)],
+                    W.BitSpec(la_p=0.4, ca_p=0.5), num_layers=2, num_q_heads=4,
+                    num_kv_heads=2, head_dim=8, tile=16, page=8),
+    # tile 16, page 4 (4 pages per tile), one-token documents
+    W.custom_config("rg_p4", [([1, 17, 40, 1], 3), ([5, 5], 16)],
+                    W.BitSpec(la_p=0.5, ca_p=0.3, la_window=1, ca_first_page=True),
+                    num_layers=1, num_q_heads=2, num_kv_heads=1, head_dim=8, tile=16, page=4),
+    # page = tile (ragged lengths only)
+    W.custom_config("rg_eq", [([50, 31, 64], 1)], W.BitSpec(la_p=0.3, ca_p=0.6),
+                    num_layers=1, num_q_heads=4, num_kv_heads=2, head_dim=8, tile=16),
+    # page = 2 and 4 tiles; documents longer than 64 tiles (two LA words per row)
+    W.custom_config("rg_p32", [([16 * 70 + 3, 45], 10)], W.BitSpec(la_p=0.1, ca_p=0.5),
+                    num_layers=1, num_q_heads=2, num_kv_heads=1, head_dim=4, tile=16, page=32),
+    W.custom_config("rg_p64", [([200, 130, 64], 0), ([77], 5)],
+                    W.BitSpec(head_density=(0.1, 0.7)), num_layers=2, num_q_heads=4,
+                    num_kv_heads=2, head_dim=4, tile=16, page=64),
+    # 65 pages (8 * 64 + 3 tokens): the CA block of each (layer, head) takes two words
+    W.custom_config("rg_cross", [([8 * 64 + 3, 20], 4)], W.BitSpec(la_p=0.2, ca_p=0.5),
+                    num_layers=2, num_q_heads=4, num_kv_heads=2, head_dim=4, tile=16, page=8),
+]
+
+
+@pytest.mark.parametrize("cfg", RAGGED_CFGS, ids=lambda c: c.name)
+def test_ragged_lists_token_rule_and_numpy_mask_agree(cfg):
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    assert not lay.aligned or cfg.name == "rg_eq"
+    qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
+    T, B = lay.total_tokens, lay.tile
+    tok = np.arange(T)
+    # query tiles: every segment cut from its own start, in token order
+    exp = []
+    for s0, e0, _ in lay.segments():
+        exp += [[x, min(B, e0 - x)] for x in range(s0, e0, B)]
+    assert qt.tolist() == exp
+    for l in range(lay.num_layers):
+        for h in range(lay.num_kv_heads):
+            A = expand_lists(lay, qt, kv, cnt, l, h)
+            Bm = oracle.key_mask(lay, la, ca, l, h, tok, tok)
+            C = oracle.token_mask(lay, la, ca, l, h)
+            assert np.array_equal(A, Bm), (l, h)
+            assert np.array_equal(Bm, C), (l, h)
+            for q, (x, rows) in enumerate(qt):
+                firsts = kv[l, h, q, :cnt[l, h, q], 0]
+                assert np.all(np.diff(firsts) > 0), "lists ascend by first token"
+                assert firsts[-1] == x and (kv[l, h, q, cnt[l, h, q] - 1, 1] >> 8) & 1 == 1
+                assert np.all((kv[l, h, q, :cnt[l, h, q] - 1, 1] >> 8) & 1 == 0)
+
+
+@pytest.mark.parametrize("name", ["pin_a", "pin_b", "pin_skew"])
+def test_ragged_decode_reduces_to_aligned_decode(name):
+    """With page == tile and every boundary a multiple of the tile, the ragged lists are
+    the aligned lists: first token = global tile index * tile, full tiles, causal last."""
+    cfgs = {
+        "pin_a": W.custom_config("pin_a", [([256, 512, 128], 128)], W.BitSpec(la_p=0.3, ca_p=0.4),
+                                 num_layers=2, num_q_heads=4, num_kv_heads=2, head_dim=16,
+                                 tile=64),
+        "pin_b": W.custom_config("pin_b", [([128, 64], 64), ([192], 0), ([], 128)],
+                                 W.BitSpec(la_p=0.5, ca_p=0.5, la_window=1, ca_first_page=True),
+                                 num_layers=1, num_q_heads=6, num_kv_heads=3, head_dim=8,
+                                 tile=64),
+        "pin_skew": W.custom_config("pin_skew", [([512] * 4, 64)],
+                                    W.BitSpec(head_density=(0.05, 0.6)), num_layers=3,
+                                    num_q_heads=4, num_kv_heads=2, head_dim=8, tile=64),
+    }
+    cfg = cfgs[name]
+    lay = W.make_layout(cfg)
+    assert lay.aligned
+    la, ca = W.make_bits(cfg, lay)
+    kv_a, cnt_a = oracle.decode(lay, la, ca)
+    qt, kv_r, cnt_r = oracle.decode_ragged(lay, la, ca)
+    B = lay.tile
+    assert qt.tolist() == [[i * B, B] for i in range(lay.num_tiles)]
+    assert np.array_equal(cnt_a, cnt_r)
+    full = B | (1 << 16)
+    for l in range(lay.num_layers):
+        for h in range(lay.num_kv_heads):
+            for i in range(lay.num_tiles):
+                n = cnt_a[l, h, i]
+                assert np.array_equal(kv_r[l, h, i, :n, 0], kv_a[l, h, i, :n] * B)
+                info = kv_r[l, h, i, :n, 1]
+                assert np.all(info[:-1] == full) and info[-1] == full | (1 << 8)
+
+
+@pytest.mark.parametrize("page,tile", [(32, 8), (4, 16), (8, 8), (2, 16)])
+def test_single_ca_bit_covers_exactly_its_page(page, tile):
+    """One CA bit of the first document admits exactly the keys of its page -- tokens
+    [j*page, (j+1)*page) of that document, cut at the document's end -- to every query
+    of the second document, whatever the tile size."""
+    n0 = 3 * page + page // 2 + 1          # a partial last page
+    cfg = W.custom_config("pg", [([n0, 2 * tile + 3], 0)], W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=4, tile=tile, page=page)
+    lay = W.make_layout(cfg)
+    C = lay.doc_pages(0)
+    for j in range(C):
+        la = np.zeros(lay.la_words_len, np.uint64)
+        ca = np.zeros(lay.ca_words_len, np.uint64)
+        ca[lay.ca_off[0]] = np.uint64(1 << j)
+        q = np.arange(n0, lay.total_tokens)
+        M = oracle.key_mask(lay, la, ca, 0, 0, q, np.arange(n0))
+        want = np.zeros(n0, bool)
+        want[j * page: min((j + 1) * page, n0)] = True
+        assert np.all(M == want[None, :]), (page, tile, j)
+        qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
+        A = expand_lists(lay, qt, kv, cnt, 0, 0)
+        assert np.array_equal(A[n0:, :n0], np.broadcast_to(want, (len(q), n0)))
+
+
+def test_ragged_decode_rejects_pages_that_do_not_nest():
+    cfg = W.custom_config("bad", [([40], 8)], W.BitSpec(pattern="ones"), num_q_heads=2,
+                          num_kv_heads=1, head_dim=4, tile=16, page=12)
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    with pytest.raises(ValueError):
+        oracle.decode_ragged(lay, la, ca)
+    cfg = W.custom_config("bad2", [([40], 8)], W.BitSpec(pattern="ones"), num_q_heads=2,
+                          num_kv_heads=1, head_dim=4, tile=64, page=2)   # 32 pages per tile
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    with pytest.raises(ValueError):
+        oracle.decode_ragged(lay, la, ca)
+
+
+# ---- attention on ragged layouts ---------------------------------------------------
+
+def _qkv(cfg, seed=0):
+    return W.make_qkv(cfg, seed)
+
+
+def _sdpa(q, k, v, mask, scale):
+    """fp64 SDPA per query head with kv head qh // G; mask [T, T] bool."""
+    qf, kf, vf = (t.double() for t in (q, k, v))
+    G = q.shape[1] // k.shape[1]
+    out = torch.zeros_like(qf)
+    for qh in range(q.shape[1]):
+        h = qh // G
+        out[:, qh] = torch.nn.functional.scaled_dot_product_attention(
+            qf[None, None, :, qh], kf[None, None, :, h], vf[None, None, :, h],
+            attn_mask=torch.from_numpy(mask)[None, None], scale=scale)[0, 0]
+    return out.numpy()
+
+
+RG_ATT = W.custom_config("rg_att", [([37, 16 * 2 + 9, 5], 11), ([23], 0), ([], 19)],
+                         W.BitSpec(la_p=0.5, ca_p=0.5), num_q_heads=4, num_kv_heads=2,
+                         head_dim=8, tile=16, page=8)
+
+
+def _prompt_causal(lay):
+    T = lay.total_tokens
+    M = np.zeros((T, T), bool)
+    for p in range(lay.num_prompts):
+        a, b = int(lay.cu_seqlens[p]), int(lay.cu_seqlens[p + 1])
+        M[a:b, a:b] = np.tril(np.ones((b - a, b - a), bool))
+    return M
+
+
+def test_ragged_all_ones_is_dense_causal_per_prompt():
+    cfg = W.custom_config("rg_ones", RG_ATT.prompts, W.BitSpec(pattern="ones"), num_q_heads=4,
+                          num_kv_heads=2, head_dim=8, tile=16, page=8)
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    q, k, v = _qkv(cfg)
+    O, _ = oracle.attention_all(lay, la, ca, 0, q, k, v, scale=0.3)
+    ref = _sdpa(q, k, v, _prompt_causal(lay), 0.3)
+    np.testing.assert_allclose(O, ref, atol=1e-12)
+
+
+def test_ragged_all_zeros_is_own_document_tile_plus_dense_suffix():
+    """No bits: a document token sees the causal keys of its own document tile (tiles cut
+    from the document start), a suffix token its whole prompt."""
+    cfg = W.custom_config("rg_zero", RG_ATT.prompts, W.BitSpec(pattern="zeros"), num_q_heads=4,
+                          num_kv_heads=2, head_dim=8, tile=16, page=8)
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    q, k, v = _qkv(cfg)
+    T, B = lay.total_tokens, lay.tile
+    M = np.zeros((T, T), bool)
+    for s0, e0, g in lay.segments():
+        for t in range(s0, e0):
+            if g < 0:
+                p = int(np.searchsorted(lay.cu_seqlens, t, side="right")) - 1
+                M[t, int(lay.cu_seqlens[p]): t + 1] = True
+            else:
+                M[t, s0 + (t - s0) // B * B: t + 1] = True
+    O, _ = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    ref = _sdpa(q, k, v, M, 1.0 / np.sqrt(8))
+    np.testing.assert_allclose(O, ref, atol=1e-12)
+
+
+def test_ragged_random_bits_match_numpy_brute_force():
+    lay = W.make_layout(RG_ATT)
+    la, ca = W.make_bits(RG_ATT, lay)
+    q, k, v = _qkv(RG_ATT)
+    O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    Ob, LSEb = oracle.brute_force_attention(lay, la, ca, 0, q, k, v)
+    np.testing.assert_allclose(O, Ob, atol=1e-12)
+    np.testing.assert_allclose(LSE, LSEb, atol=1e-12)

@@ -17,8 +17,13 @@ Bit layout (the pages give none; this is the reading used everywhere):
     (layer l, kv head h) is a T_g x W_g row-major array of uint64 words at
     word offset ``la_off[g] + (l*Hkv + h) * T_g * W_g``.  Bit j of row i is
     bit (j & 63) (LSB first) of word (j >> 6); only j < i is meaningful.
-  * CA block of document g for (l, h) is W_g words at
-    ``ca_off[g] + (l*Hkv + h) * W_g``; bit j marks KV page j of document g.
+  * CA block of document g for (l, h) is V_g = ceil(C_g/64) words at
+    ``ca_off[g] + (l*Hkv + h) * V_g``; bit j marks KV page j of document g.
+  * Tiles and pages are counted from the document's own first token:
+    T_g = ceil(n_g / tile) LA tiles and C_g = ceil(n_g / page) CA pages for a
+    document of n_g tokens, the last ones possibly partial.  With page == tile
+    and every length a multiple of the tile (the default workloads) both
+    counts are n_g / tile and V_g = W_g.
 """
 from __future__ import annotations
 
@@ -73,10 +78,15 @@ class Config:
     prompts: tuple
     bits: BitSpec
     description: str = ""
+    page: int = 0  # CA page size in tokens; 0 = the tile size
 
     @property
     def total_tokens(self) -> int:
         return sum(sum(d) + s for d, s in self.prompts)
+
+    @property
+    def page_size(self) -> int:
+        return self.page if self.page > 0 else self.tile
 
 
 @dataclasses.dataclass
@@ -98,14 +108,48 @@ class Layout:
     ca_off: np.ndarray       # int64 [D]   word offset of each doc's CA blocks
     la_words_len: int
     ca_words_len: int
+    page: int = 0  # CA page size in tokens; 0 = the tile size
+
+    @property
+    def page_size(self) -> int:
+        return self.page if self.page > 0 else self.tile
 
     @property
     def num_tiles(self) -> int:
         return self.total_tokens // self.tile
 
+    @property
+    def aligned(self) -> bool:
+        """page == tile and every prompt and document boundary a multiple of the tile."""
+        B = self.tile
+        return (self.page_size == B and all(int(x) % B == 0 for x in self.cu_seqlens)
+                and all(int(x) % B == 0 for x in self.doc_end))
+
+    def segments(self):
+        """(start, end, document or -1 for the query suffix) of every segment, in token order."""
+        out = []
+        for p in range(self.num_prompts):
+            pos = int(self.cu_seqlens[p])
+            for g in range(int(self.doc_cu[p]), int(self.doc_cu[p + 1])):
+                out.append((pos, int(self.doc_end[g]), g))
+                pos = int(self.doc_end[g])
+            out.append((pos, int(self.cu_seqlens[p + 1]), -1))
+        return out
+
+    @property
+    def num_query_tiles(self) -> int:
+        """Query tiles counted per segment (documents and suffixes tile from their own start)."""
+        B = self.tile
+        return sum((e - s + B - 1) // B for s, e, _ in self.segments())
+
     def doc_tiles(self, g: int) -> int:
         start = self.doc_start(g)
-        return (int(self.doc_end[g]) - start) // self.tile
+        return (int(self.doc_end[g]) - start + self.tile - 1) // self.tile
+
+    def doc_pages(self, g: int) -> int:
+        start = self.doc_start(g)
+        P = self.page_size
+        return (int(self.doc_end[g]) - start + P - 1) // P
 
     def doc_start(self, g: int) -> int:
         p = int(np.searchsorted(self.doc_cu, g, side="right")) - 1
@@ -113,10 +157,10 @@ class Layout:
 
 
 def custom_config(name, prompts, bits, num_layers=1, num_q_heads=4, num_kv_heads=2,
-                  head_dim=128, tile=128, description="") -> Config:
+                  head_dim=128, tile=128, description="", page=0) -> Config:
     prompts = tuple((tuple(int(x) for x in docs), int(suf)) for docs, suf in prompts)
     return Config(name, num_layers, num_q_heads, num_kv_heads, head_dim, tile, prompts,
-                  bits, description)
+                  bits, description, int(page))
 
 
 def _batch4(p: float) -> Config:
@@ -164,6 +208,7 @@ def get_config(name: str) -> Config:
 
 def make_layout(cfg: Config) -> Layout:
     B = cfg.tile
+    Pg = cfg.page_size
     cu = [0]
     doc_cu = [0]
     doc_end = []
@@ -171,28 +216,31 @@ def make_layout(cfg: Config) -> Layout:
     la_pos = ca_pos = 0
     max_tiles = 0
     for docs, suf in cfg.prompts:
-        start = cu[-1]
-        pos = start
+        pos = cu[-1]
+        tiles = (suf + B - 1) // B  # key tiles of the prompt, each segment tiled on its own
         for n in docs:
-            T = n // B
+            T = (n + B - 1) // B
             W = (T + 63) // 64
+            V = ((n + Pg - 1) // Pg + 63) // 64
+            tiles += T
             pos += n
             doc_end.append(pos)
             la_off.append(la_pos)
             ca_off.append(ca_pos)
             la_pos += cfg.num_layers * cfg.num_kv_heads * T * W
-            ca_pos += cfg.num_layers * cfg.num_kv_heads * W
+            ca_pos += cfg.num_layers * cfg.num_kv_heads * V
         pos += suf
         cu.append(pos)
         doc_cu.append(len(doc_end))
-        max_tiles = max(max_tiles, (pos - start) // B)
+        max_tiles = max(max_tiles, tiles)
     return Layout(
         num_prompts=len(cfg.prompts), num_docs=len(doc_end), num_layers=cfg.num_layers,
         num_q_heads=cfg.num_q_heads, num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim,
         tile=B, total_tokens=cu[-1], max_tiles_per_prompt=max(max_tiles, 1),
         cu_seqlens=np.asarray(cu, np.int32), doc_cu=np.asarray(doc_cu, np.int32),
         doc_end=np.asarray(doc_end, np.int32), la_off=np.asarray(la_off, np.int64),
-        ca_off=np.asarray(ca_off, np.int64), la_words_len=la_pos, ca_words_len=ca_pos)
+        ca_off=np.asarray(ca_off, np.int64), la_words_len=la_pos, ca_words_len=ca_pos,
+        page=cfg.page)
 
 
 def _pack_rows(bits: np.ndarray) -> np.ndarray:
@@ -225,37 +273,39 @@ def make_bits(cfg: Config, layout: Layout):
         la_p, ca_p = spec.la_p, spec.ca_p
     for g in range(layout.num_docs):
         T = layout.doc_tiles(g)
+        C = layout.doc_pages(g)
         W = (T + 63) // 64
+        V = (C + 63) // 64
         i = np.arange(T)[:, None]
         j = np.arange(T)[None, :]
         below = j < i
         if spec.pattern == "random":
             rng = np.random.Generator(np.random.PCG64(seed_for(cfg.name, "doc", g, "bits")))
             la_b = rng.random((L, Hkv, T, T)) < la_p
-            ca_b = rng.random((L, Hkv, T)) < ca_p
+            ca_b = rng.random((L, Hkv, C)) < ca_p
             if spec.la_window > 0:
                 la_b |= ((i - j) >= 1) & ((i - j) <= spec.la_window)
-            if spec.ca_first_page and T > 0:
+            if spec.ca_first_page and C > 0:
                 ca_b[..., 0] = True
         elif spec.pattern == "ones":
             la_b = np.ones((L, Hkv, T, T), bool)
-            ca_b = np.ones((L, Hkv, T), bool)
+            ca_b = np.ones((L, Hkv, C), bool)
         elif spec.pattern == "zeros":
             la_b = np.zeros((L, Hkv, T, T), bool)
-            ca_b = np.zeros((L, Hkv, T), bool)
+            ca_b = np.zeros((L, Hkv, C), bool)
         elif spec.pattern == "la_only":
             la_b = np.ones((L, Hkv, T, T), bool)
-            ca_b = np.zeros((L, Hkv, T), bool)
+            ca_b = np.zeros((L, Hkv, C), bool)
         elif spec.pattern == "ca_only":
             la_b = np.zeros((L, Hkv, T, T), bool)
-            ca_b = np.ones((L, Hkv, T), bool)
+            ca_b = np.ones((L, Hkv, C), bool)
         else:
             raise ValueError(spec.pattern)
         # only the strictly-lower triangle of an LA block carries meaning; the
         # generator leaves the rest clear so that stored words stay canonical
         la_b = la_b & below
         la[layout.la_off[g]: layout.la_off[g] + L * Hkv * T * W] = _pack_rows(la_b).reshape(-1)
-        ca[layout.ca_off[g]: layout.ca_off[g] + L * Hkv * W] = _pack_rows(ca_b).reshape(-1)
+        ca[layout.ca_off[g]: layout.ca_off[g] + L * Hkv * V] = _pack_rows(ca_b).reshape(-1)
     return la, ca
 
 
