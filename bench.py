@@ -469,6 +469,9 @@ def run_ours(args, cfg):
         result["density_sweep"] = run_sweep(args, dev, stream)
     del qkv, outs
     torch.cuda.empty_cache()
+    if not args.no_ragged and rank == 0 and world == 1 and not args.layers:
+        result["ragged"] = run_ragged(args, dev, stream)
+        torch.cuda.empty_cache()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
@@ -606,6 +609,89 @@ def run_sweep(args, dev, stream):
     return rows
 
 
+def run_ragged(args, dev, stream):
+    """The general-layout step on the ragged 33K workload: sift_decode_ragged of all layers,
+    then one sift_sparse_prefill_ragged per layer; dense causal attention over the same
+    prompts (documents play no part in it) is timed beside it."""
+    import torch
+    import bit_vector_guided_gb300 as sift
+    cfg = W.get_config("llama_32k_ragged")
+    L = cfg.num_layers
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, dev)
+    la_d = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).to(dev)
+    ca_d = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).to(dev)
+    qkv = [W.make_qkv(cfg, l, device=dev) for l in range(L)]
+    o = torch.empty_like(qkv[0][0])
+    lse = torch.empty((cfg.num_q_heads, lay.total_tokens), dtype=torch.float32, device=dev)
+    st = prob.new_status()
+    ws = prob.new_workspace()
+    H, NQ, R = cfg.num_kv_heads, prob.num_query_tiles, prob.max_tiles_per_prompt
+    qt = torch.empty((NQ, 2), dtype=torch.int32, device=dev)
+    kv = torch.empty((L, H, NQ, R, 2), dtype=torch.int32, device=dev)
+    cnt = torch.empty((L, H, NQ), dtype=torch.int32, device=dev)
+    sch = torch.empty((L, H * NQ), dtype=torch.int32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(L + 2)]
+
+    def step(record=False):
+        if record:
+            ev[0].record(stream)
+        sift.decode_ragged(prob, la_d, ca_d, qt, kv, cnt, sch, dev_status=st, stream=stream)
+        if record:
+            ev[1].record(stream)
+        for l in range(L):
+            q, k, v = qkv[l]
+            sift.sparse_prefill_ragged(prob, l, q, k, v, qt, kv, cnt, sch, 0.0, o, lse, ws, st,
+                                       stream)
+            if record:
+                ev[2 + l].record(stream)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = 3
+    layer_ms, dec_ms, step_ms = [], [], []
+    for _ in range(steps):
+        step(record=True)
+        torch.cuda.synchronize(dev)
+        dec_ms.append(ev[0].elapsed_time(ev[1]))
+        layer_ms += [ev[1 + l].elapsed_time(ev[2 + l]) for l in range(L)]
+        step_ms.append(ev[0].elapsed_time(ev[L + 1]))
+    if int(st.item()) != 0:
+        raise RuntimeError("ragged device status " + sift.status_string(int(st.item())))
+    fl = computed_flops(cfg, cnt.cpu().numpy())
+    kern_ms = float(np.mean(layer_ms))
+    # dense causal attention over the same prompts: an aligned problem without documents
+    dprob = sift.SiftProblem(cu_seqlens=lay.cu_seqlens,
+                             doc_cu=np.zeros(lay.num_prompts + 1, np.int32), doc_end=[],
+                             la_off=[], ca_off=[], num_layers=1, num_q_heads=cfg.num_q_heads,
+                             num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim,
+                             tile=cfg.tile, la_words_len=0, ca_words_len=0, device=dev)
+    dws = dprob.new_workspace()
+    q, k, v = qkv[0]
+    for _ in range(2):
+        sift.dense_prefill(dprob, q, k, v, 0.0, o, lse, dws, st, stream)
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    d0.record(stream)
+    for _ in range(3):
+        sift.dense_prefill(dprob, q, k, v, 0.0, o, lse, dws, st, stream)
+    d1.record(stream)
+    torch.cuda.synchronize(dev)
+    dense_ms = d0.elapsed_time(d1) / 3
+    peaks, _ = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    ktf = float(fl.mean()) / (kern_ms * 1e-3) / 1e12
+    return {"workload": cfg.name, "page": cfg.page, "query_tiles": NQ,
+            "ms_per_step": float(np.mean(step_ms)),
+            "tflops": float(fl.sum()) / (float(np.mean(step_ms)) * 1e-3) / 1e12,
+            "sparse_ms_per_layer": kern_ms, "kernel_tflops": ktf,
+            "kernel_frac_of_peak": ktf / peak,
+            "decode_us": 1e3 * float(np.median(dec_ms)),
+            "dense_ms_per_layer": dense_ms, "speedup_vs_dense": dense_ms / kern_ms,
+            "gpu_launches_per_step": 3 + L}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -616,6 +702,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-ragged", action="store_true",
+                    help="skip the general-layout leg (ragged documents, 16-token CA pages)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
                     help="N > 1: every rank runs the whole workload (replicas, weak scaling) "

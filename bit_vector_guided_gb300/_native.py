@@ -18,6 +18,7 @@ from . import build as _build
 
 __all__ = ["SiftError", "SiftProblem", "load_library", "decode", "sparse_prefill",
            "dense_prefill", "dense_prefill_noalloc", "fused_prefill", "build_bits",
+           "decode_ragged", "sparse_prefill_ragged",
            "build_bits_workspace_bytes", "workspace_bytes", "status_string", "debug_set_waits",
            "abi_version", "exported_symbols", "STATUS"]
 
@@ -36,7 +37,7 @@ class _Problem(ctypes.Structure):
                 ("num_layers", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
                 ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("tile", ctypes.c_int32), ("total_tokens", ctypes.c_int32),
-                ("max_tiles_per_prompt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("max_tiles_per_prompt", ctypes.c_int32), ("page", ctypes.c_int32),
                 ("cu_seqlens", ctypes.c_void_p), ("doc_cu", ctypes.c_void_p),
                 ("doc_end", ctypes.c_void_p), ("la_off", ctypes.c_void_p),
                 ("ca_off", ctypes.c_void_p), ("la_words_len", ctypes.c_int64),
@@ -74,6 +75,11 @@ def load_library(path: Optional[str] = None):
     lib.sift_build_bits_workspace_bytes.restype = sz
     lib.sift_build_bits.argtypes = [P, i32, P, P, i32, f32, f32, f32, P, P, P, sz, P, P]
     lib.sift_build_bits.restype = i32
+    lib.sift_decode_ragged.argtypes = [P, i32, P, P, P, P, P, P, P, P]
+    lib.sift_decode_ragged.restype = i32
+    lib.sift_sparse_prefill_ragged.argtypes = [P, i32, i32, P, P, P, P, P, P, P, f32, P, P, P,
+                                               sz, P, P]
+    lib.sift_sparse_prefill_ragged.restype = i32
     lib.sift_status_string.argtypes = [i32]
     lib.sift_status_string.restype = ctypes.c_char_p
     lib.sift_debug_set_waits.argtypes = [u64, i32]
@@ -127,7 +133,7 @@ class SiftProblem:
 
     def __init__(self, *, cu_seqlens, doc_cu, doc_end, la_off, ca_off, num_layers, num_q_heads,
                  num_kv_heads, head_dim, tile, la_words_len, ca_words_len,
-                 max_tiles_per_prompt: Optional[int] = None, device="cuda"):
+                 max_tiles_per_prompt: Optional[int] = None, page: int = 0, device="cuda"):
         import torch
         cu = np.asarray(cu_seqlens, np.int32)
         self.num_prompts = len(cu) - 1
@@ -139,6 +145,20 @@ class SiftProblem:
         self.tile = int(tile)
         self.total_tokens = int(cu[-1])
         self.num_tiles = self.total_tokens // self.tile
+        self.page = int(page)
+        # query tiles counted per segment (documents and suffixes tile from their own start),
+        # the row count of the general-layout entry points
+        dcu = np.asarray(doc_cu, np.int64)
+        dend = np.asarray(doc_end, np.int64)
+        B = self.tile
+        nq = 0
+        for p in range(self.num_prompts):
+            pos = int(cu[p])
+            for g in range(int(dcu[p]), int(dcu[p + 1])):
+                nq += (int(dend[g]) - pos + B - 1) // B
+                pos = int(dend[g])
+            nq += (int(cu[p + 1]) - pos + B - 1) // B
+        self.num_query_tiles = nq
         if max_tiles_per_prompt is None:
             max_tiles_per_prompt = int(np.max(np.diff(cu)) // self.tile) if len(cu) > 1 else 1
         self.max_tiles_per_prompt = max(int(max_tiles_per_prompt), 1)
@@ -159,7 +179,7 @@ class SiftProblem:
         self.ca_words_len = int(ca_words_len)
         self._struct = _Problem(self.num_prompts, self.num_docs, self.num_layers,
                                 self.num_q_heads, self.num_kv_heads, self.head_dim, self.tile,
-                                self.total_tokens, self.max_tiles_per_prompt, 0,
+                                self.total_tokens, self.max_tiles_per_prompt, self.page,
                                 _ptr(self._cu), _ptr(self._doc_cu), _ptr(self._doc_end),
                                 _ptr(self._la_off), _ptr(self._ca_off), self.la_words_len,
                                 self.ca_words_len)
@@ -172,7 +192,8 @@ class SiftProblem:
                    num_q_heads=layout.num_q_heads, num_kv_heads=layout.num_kv_heads,
                    head_dim=layout.head_dim, tile=layout.tile,
                    la_words_len=layout.la_words_len, ca_words_len=layout.ca_words_len,
-                   max_tiles_per_prompt=layout.max_tiles_per_prompt, device=device)
+                   max_tiles_per_prompt=layout.max_tiles_per_prompt,
+                   page=int(getattr(layout, "page", 0) or 0), device=device)
 
     @property
     def ref(self):
@@ -330,3 +351,52 @@ def build_bits(prob: SiftProblem, layer: int, q, k, max_doc_tiles: int, la_fract
                              int(workspace.numel()), _ptr(dev_status), _stream(stream))
     _check(rc, "sift_build_bits")
     return la_words, ca_words
+
+
+def decode_ragged(prob: SiftProblem, la_words, ca_words, qtiles=None, kv=None, counts=None,
+                  sched=None, dev_status=None, stream=None):
+    """sift_decode_ragged: returns (qtiles [NQ,2], kv [L,Hkv,NQ,rowcap,2], counts [L,Hkv,NQ],
+    sched [L,Hkv*NQ]) for documents of any length and a CA page size of their own."""
+    import torch
+    lib = load_library()
+    L, H, NQ, R = prob.num_layers, prob.num_kv_heads, prob.num_query_tiles, prob.max_tiles_per_prompt
+    dev = prob.device
+    if qtiles is None:
+        qtiles = torch.empty((NQ, 2), dtype=torch.int32, device=dev)
+    if kv is None:
+        kv = torch.empty((L, H, NQ, R, 2), dtype=torch.int32, device=dev)
+    if counts is None:
+        counts = torch.empty((L, H, NQ), dtype=torch.int32, device=dev)
+    if sched is None:
+        sched = torch.empty((L, H * NQ), dtype=torch.int32, device=dev)
+    if dev_status is None:
+        dev_status = prob.new_status()
+    rc = lib.sift_decode_ragged(prob.ref, NQ, _ptr(la_words), _ptr(ca_words), _ptr(qtiles),
+                                _ptr(kv), _ptr(counts), _ptr(sched), _ptr(dev_status),
+                                _stream(stream))
+    _check(rc, "sift_decode_ragged")
+    return qtiles, kv, counts, sched
+
+
+def sparse_prefill_ragged(prob: SiftProblem, layer: int, q, k, v, qtiles, kv, counts, sched,
+                          softmax_scale: float = 0.0, o=None, lse=None, workspace=None,
+                          dev_status=None, stream=None):
+    """sift_sparse_prefill_ragged: returns (o bf16 [T,Hq,d], lse fp32 [Hq,T])."""
+    import torch
+    lib = load_library()
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((prob.num_q_heads, prob.total_tokens), dtype=torch.float32,
+                          device=q.device)
+    if workspace is None:
+        workspace = prob.new_workspace()
+    if dev_status is None:
+        dev_status = prob.new_status()
+    rc = lib.sift_sparse_prefill_ragged(prob.ref, prob.num_query_tiles, int(layer), _ptr(q),
+                                        _ptr(k), _ptr(v), _ptr(qtiles), _ptr(kv), _ptr(counts),
+                                        _ptr(sched), float(softmax_scale), _ptr(o), _ptr(lse),
+                                        _ptr(workspace), int(workspace.numel()), _ptr(dev_status),
+                                        _stream(stream))
+    _check(rc, "sift_sparse_prefill_ragged")
+    return o, lse

@@ -20,6 +20,7 @@ sift_status validate_problem(const sift_problem *p, bool attention) {
         return SIFT_ERR_INVALID_ARG;
     if (p->num_q_heads % p->num_kv_heads != 0) return SIFT_ERR_INVALID_ARG;
     if (p->total_tokens % p->tile != 0) return SIFT_ERR_UNSUPPORTED;
+    if (p->page != 0 && p->page != p->tile) return SIFT_ERR_UNSUPPORTED;
     if (p->cu_seqlens == nullptr || p->doc_cu == nullptr) return SIFT_ERR_INVALID_ARG;
     if (p->num_docs > 0 && (p->doc_end == nullptr || p->la_off == nullptr || p->ca_off == nullptr))
         return SIFT_ERR_INVALID_ARG;
@@ -35,6 +36,42 @@ sift_status validate_problem(const sift_problem *p, bool attention) {
             return SIFT_ERR_UNSUPPORTED;
     }
     return SIFT_OK;
+}
+
+static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+sift_status validate_ragged(const sift_problem *p, bool attention) {
+    if (p == nullptr) return SIFT_ERR_INVALID_ARG;
+    if (p->num_prompts < 1 || p->num_docs < 0 || p->num_layers < 1 || p->num_q_heads < 1 ||
+        p->num_kv_heads < 1 || p->tile < 1 || p->total_tokens < 1 ||
+        p->max_tiles_per_prompt < 1 || p->la_words_len < 0 || p->ca_words_len < 0 ||
+        p->page < 0)
+        return SIFT_ERR_INVALID_ARG;
+    if (p->num_q_heads % p->num_kv_heads != 0) return SIFT_ERR_INVALID_ARG;
+    if (p->cu_seqlens == nullptr || p->doc_cu == nullptr) return SIFT_ERR_INVALID_ARG;
+    if (p->num_docs > 0 && (p->doc_end == nullptr || p->la_off == nullptr || p->ca_off == nullptr))
+        return SIFT_ERR_INVALID_ARG;
+    // the list format holds a tile's length in 8 bits and at most 16 page bits
+    if (!pow2(p->tile) || p->tile < 8 || p->tile > 128) return SIFT_ERR_UNSUPPORTED;
+    const int page = p->page ? p->page : p->tile;
+    if (!pow2(page) || page < p->tile / 16 || page > (1 << 24)) return SIFT_ERR_UNSUPPORTED;
+    if (p->max_tiles_per_prompt > 49152) return SIFT_ERR_INVALID_ARG;
+    const int64_t cap = max_query_tiles(p);
+    if (cap * p->num_kv_heads > INT32_MAX / 2) return SIFT_ERR_UNSUPPORTED;
+    if (attention) {
+        if (p->head_dim != 64 && p->head_dim != 128) return SIFT_ERR_UNSUPPORTED;
+        if (p->tile != 64 && p->tile != 128) return SIFT_ERR_UNSUPPORTED;
+        if ((p->num_q_heads / p->num_kv_heads) % 2 != 0) return SIFT_ERR_UNSUPPORTED;
+        if (static_cast<int64_t>(p->total_tokens) * p->num_q_heads * p->head_dim > INT32_MAX * 8ll)
+            return SIFT_ERR_UNSUPPORTED;
+    }
+    return SIFT_OK;
+}
+
+int64_t max_query_tiles(const sift_problem *p) {
+    // each segment (documents and suffixes) adds at most one partial tile
+    return (static_cast<int64_t>(p->total_tokens) + p->tile - 1) / p->tile + p->num_docs +
+           p->num_prompts;
 }
 
 int device_sm_count() {
@@ -65,8 +102,13 @@ const char *sift_status_string(sift_status s) {
 }
 
 size_t sift_workspace_bytes(const sift_problem *p) {
-    if (sift::validate_problem(p, false) != SIFT_OK) return 0;
-    const size_t units = static_cast<size_t>(p->total_tokens / p->tile) * p->num_kv_heads;
+    size_t units = 0;
+    if (sift::validate_problem(p, false) == SIFT_OK)
+        units = static_cast<size_t>(p->total_tokens / p->tile) * p->num_kv_heads;
+    else if (sift::validate_ragged(p, false) == SIFT_OK)
+        units = static_cast<size_t>(sift::max_query_tiles(p)) * p->num_kv_heads;
+    else
+        return 0;
     return sift::kWsHeader + 2 * units * sizeof(int32_t);
 }
 
@@ -75,6 +117,6 @@ void sift_debug_set_waits(uint64_t wait_timeout_ns, int32_t stall_flag) {
     sift::g_stall.store(stall_flag);
 }
 
-int32_t sift_abi_version(void) { return 100; }
+int32_t sift_abi_version(void) { return 101; }
 
 }  // extern "C"

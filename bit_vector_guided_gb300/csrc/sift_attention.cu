@@ -56,6 +56,7 @@ constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all
 constexpr int kModeList = 0;   // decoded lists in HBM (sift_sparse_prefill)
 constexpr int kModeDense = 1;  // implicit {prompt start .. i} (sift_dense_prefill)
 constexpr int kModeBits = 2;   // the LA/CA bits themselves, walked on the fly (sift_fused_prefill)
+constexpr int kModeRagged = 3; // (first token, info) lists of a general layout (sift_sparse_prefill_ragged)
 constexpr int kMaxFusedPrompts = 64;
 
 struct WorkItem {
@@ -74,6 +75,8 @@ struct WorkItem {
     int32_t W;       // LA words per row of the document
     int32_t pad;
     int64_t la_row;  // word offset of the row's LA words
+    // general layout: the query tile's first token and its rows inside the segment
+    int32_t q0, qlen;
 };
 
 struct Ctl {
@@ -108,6 +111,11 @@ struct AttnParams {
     const uint64_t *la, *ca;
     int64_t la_len, ca_len;
     int32_t P, D, B, layer, Hkv;
+    // general layout (sift_sparse_prefill_ragged)
+    const int2 *kv2;         // layer slice [Hkv][NQ][rowcap] of (first token, info)
+    const int32_t *qt;       // [NQ][2] (first token, rows)
+    int32_t lp;              // log2 of min(page, tile)
+    uint32_t full_info;      // info of a whole tile with every page kept
 };
 
 template <int BT, int HD>
@@ -193,6 +201,15 @@ __device__ __forceinline__ WorkItem fetch_item(const AttnParams &p, int w) {
     it.n = n;
     it.first = it.i - n + 1;
     it.list = (static_cast<int64_t>(it.h) * p.N + it.i) * p.rowcap;
+    if constexpr (MODE == kModeRagged) {
+        it.q0 = __ldg(p.qt + 2 * it.i);
+        it.qlen = __ldg(p.qt + 2 * it.i + 1);
+        if (it.q0 < 0 || it.qlen < 0 || it.qlen > p.B || it.q0 > p.total_tokens - it.qlen) {
+            set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+            it.q0 = 0;
+            it.qlen = 0;  // computed, never stored
+        }
+    }
     it.valid = 1;
     return it;
 }
@@ -204,6 +221,14 @@ __device__ __forceinline__ int list_entry(const AttnParams &p, const WorkItem &i
     constexpr bool DENSE = MODE == kModeDense;
     if (j >= it.n) return 0;
     if (DENSE) return it.first + j;
+    if constexpr (MODE == kModeRagged) {  // the key tile's first token
+        int x = __ldg(&p.kv2[it.list + j].x);
+        if (x < 0 || x > it.q0 || (j == it.n - 1 && x != it.q0)) {
+            set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+            x = it.q0;
+        }
+        return x;
+    }
     int idx = __ldg(p.kv_idx + it.list + j);
     if (idx < 0 || idx > it.i || (j == it.n - 1 && idx != it.i)) {
         set_status(p.status, SIFT_ERR_DEVICE_CHECK);
@@ -375,6 +400,38 @@ __device__ bool walk_bits(const AttnParams &p, const WorkItem &it, uint32_t lane
     return visit(it.i);
 }
 
+// General layout: clear (to -inf) the columns of a key tile that row `row` may not use.
+// info = len | causal << 8 | mask << 16: columns c < len whose page bit c >> lp is set,
+// and c <= row on the diagonal.  Built as one 32-bit visibility word per 32 columns.
+template <int BT>
+__device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int row, int lp) {
+    const int len = static_cast<int>(info & 0xffu);
+    const bool causal = (info >> 8) & 1u;
+    const uint32_t pm = info >> 16;
+    uint32_t vis[BT / 32];
+#pragma unroll
+    for (int w = 0; w < BT / 32; ++w) {
+        const int c0 = 32 * w;
+        const uint32_t lm = len >= c0 + 32 ? kFull : (len <= c0 ? 0u : (1u << (len - c0)) - 1u);
+        uint32_t pw;
+        if (lp >= 5) {
+            pw = ((pm >> (c0 >> lp)) & 1u) ? kFull : 0u;
+        } else {
+            const int per = 32 >> lp;
+            const uint32_t ones = (1u << (1 << lp)) - 1u;
+            pw = 0u;
+            for (int k = 0; k < per; ++k)
+                if ((pm >> (w * per + k)) & 1u) pw |= ones << (k << lp);
+        }
+        uint32_t cm = kFull;
+        if (causal) cm = row >= c0 + 31 ? kFull : (row < c0 ? 0u : (2u << (row - c0)) - 1u);
+        vis[w] = lm & pw & cm;
+    }
+#pragma unroll
+    for (int c = 0; c < BT; ++c)
+        if (!((vis[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+}
+
 template <int BT, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -382,6 +439,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
     using G = Geo<BT, HD>;
     constexpr bool DENSE = MODE == kModeDense;
+    constexpr bool RAGGED = MODE == kModeRagged;  // list entries are first tokens, not tiles
     (void)DENSE;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -479,7 +537,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             if (nxt.valid && lane == 0)
                 for (int s = 0; s < 2; ++s)
                     for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_prefetch_l2_3d(&tmQ, 64 * b, nxt.hq0 + s, nxt.i * BT);
+                        ptx::tma_prefetch_l2_3d(&tmQ, 64 * b, nxt.hq0 + s,
+                                                RAGGED ? nxt.q0 : nxt.i * BT);
             auto load_k = [&](int idx) -> bool {
                 const int ks = kf % kKSlots;
                 if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
@@ -487,7 +546,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
                     for (int b = 0; b < G::kBoxes; ++b)
                         ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox, &tmK,
-                                              B_(c.k_full[ks]), 64 * b, it.h, idx * BT, pol_kv);
+                                              B_(c.k_full[ks]), 64 * b, it.h,
+                                              RAGGED ? idx : idx * BT, pol_kv);
                 }
                 ++kf;
                 return true;
@@ -531,7 +591,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 for (int s = 0; s < 2; ++s)
                     for (int b = 0; b < G::kBoxes; ++b)
                         ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
-                                              B_(c.q_full), 64 * b, it.hq0 + s, it.i * BT, pol_q);
+                                              B_(c.q_full), 64 * b, it.hq0 + s,
+                                              RAGGED ? it.q0 : it.i * BT, pol_q);
             }
             ++qk;
             auto load_v = [&](int idx) -> bool {
@@ -541,7 +602,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
                     for (int b = 0; b < G::kBoxes; ++b)
                         ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox, &tmV,
-                                              B_(c.v_full[vs]), 64 * b, it.h, idx * BT, pol_kv);
+                                              B_(c.v_full[vs]), 64 * b, it.h,
+                                              RAGGED ? idx : idx * BT, pol_kv);
                 }
                 ++vf;
                 return true;
@@ -692,6 +754,9 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 float m = -INFINITY, l = 0.f;
                 bool ok = true;
                 for (int j = 0; j < it.n; ++j) {
+                    uint32_t info = 0;  // general layout: this key tile's length / causal / pages
+                    if constexpr (RAGGED) info = static_cast<uint32_t>(__ldg(&p.kv2[it.list + j].y));
+                    (void)info;
                     if (!wait_warp(c, B_(c.s_full[s]), sph, p)) { ok = false; break; }
                     sph ^= 1;
                     if (releaser) {
@@ -703,7 +768,9 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     ptx::tc_fence_after();
                     float x[BT];
                     if constexpr (BT == 128) ptx::tmem_ld128(tS, x); else ptx::tmem_ld64(tS, x);
-                    if (j == it.n - 1) {
+                    if constexpr (RAGGED) {
+                        if (info != p.full_info) mask_columns<BT>(x, info, row, p.lp);
+                    } else if (j == it.n - 1) {
 #pragma unroll
                         for (int cidx = 0; cidx < BT; ++cidx)
                             if (cidx > row) x[cidx] = -INFINITY;
@@ -769,9 +836,13 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 if (releaser) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
                 ptx::tc_fence_after();
                 const float inv = 1.f / l;
-                const int64_t tok = static_cast<int64_t>(it.i) * BT + row;
+                const int64_t tok = RAGGED ? static_cast<int64_t>(it.q0) + row
+                                           : static_cast<int64_t>(it.i) * BT + row;
                 const int hq = it.hq0 + s;
                 uint4 *orow = reinterpret_cast<uint4 *>(p.o + (tok * p.Hq + hq) * HD);
+                // rows past the segment's end are not stored; every lane still takes part
+                // in the warp-collective tensor-memory loads
+                const bool store = !RAGGED || row < it.qlen;
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     float ov[32];
@@ -780,13 +851,16 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
                         pk[t] = ptx::pack_bf16x2(ov[2 * t] * inv, ov[2 * t + 1] * inv);
+                    if (store) {
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        orow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2],
-                                                       pk[4 * v4 + 3]);
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            orow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1],
+                                                           pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                    }
                 }
-                p.lse[static_cast<int64_t>(hq) * p.total_tokens + tok] =
-                    (m + log2f(l)) * 0.69314718055994530942f;
+                if (store)
+                    p.lse[static_cast<int64_t>(hq) * p.total_tokens + tok] =
+                        (m + log2f(l)) * 0.69314718055994530942f;
                 ptx::tc_fence_before();
             }
         }
@@ -869,8 +943,9 @@ sift_status dispatch(int tile, int hd, const CUtensorMap &mq, const CUtensorMap 
 sift_status prepare(const sift_problem *prob, const void *q, const void *k, const void *v,
                     float softmax_scale, void *o, float *lse, void *workspace,
                     size_t workspace_bytes, int32_t *dev_status, CUtensorMap *maps,
-                    AttnParams *p) {
-    sift_status st = validate_problem(prob, true);
+                    AttnParams *p, int num_query_tiles = 0) {
+    // num_query_tiles > 0: the general layout, whose query tiles are counted per segment
+    sift_status st = num_query_tiles > 0 ? validate_ragged(prob, true) : validate_problem(prob, true);
     if (st != SIFT_OK) return st;
     if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr ||
         workspace == nullptr || dev_status == nullptr)
@@ -885,7 +960,7 @@ sift_status prepare(const sift_problem *prob, const void *q, const void *k, cons
         !make_map(&maps[1], k, d, prob->num_kv_heads, T, B) ||
         !make_map(&maps[2], v, d, prob->num_kv_heads, T, B))
         return SIFT_ERR_CUDA;
-    const int N = T / B;
+    const int N = num_query_tiles > 0 ? num_query_tiles : T / B;
     const int G = prob->num_q_heads / prob->num_kv_heads;
     AttnParams a{};
     a.o = static_cast<__nv_bfloat16 *>(o);
@@ -935,6 +1010,43 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
     p.sched = sched + lu;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
     return dispatch<kModeList>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+}
+
+extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int32_t num_query_tiles,
+                                                  int32_t layer, const void *q, const void *k,
+                                                  const void *v, const int32_t *qtiles,
+                                                  const int32_t *kv, const int32_t *counts,
+                                                  const int32_t *sched, float softmax_scale,
+                                                  void *o, float *lse, void *workspace,
+                                                  size_t workspace_bytes, int32_t *dev_status,
+                                                  cudaStream_t stream) {
+    using namespace sift;
+    if (prob == nullptr || layer < 0 || layer >= prob->num_layers || qtiles == nullptr ||
+        kv == nullptr || counts == nullptr || sched == nullptr || num_query_tiles < 1 ||
+        (reinterpret_cast<uintptr_t>(kv) & 7u) != 0)
+        return SIFT_ERR_INVALID_ARG;
+    if (validate_ragged(prob, true) == SIFT_OK && num_query_tiles > max_query_tiles(prob))
+        return SIFT_ERR_INVALID_ARG;
+    CUtensorMap maps[3];
+    AttnParams p;
+    sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
+                             dev_status, maps, &p, num_query_tiles);
+    if (st != SIFT_OK) return st;
+    const int64_t lu = static_cast<int64_t>(layer) * p.U;
+    p.kv2 = reinterpret_cast<const int2 *>(kv) + lu * p.rowcap;
+    p.counts = counts + lu;
+    p.sched = sched + lu;
+    p.qt = qtiles;
+    p.B = prob->tile;
+    const int page = prob->page ? prob->page : prob->tile;
+    const int pin = page < prob->tile ? page : prob->tile;
+    int lp = 0;
+    while ((1 << lp) < pin) ++lp;
+    p.lp = lp;
+    p.full_info = static_cast<uint32_t>(prob->tile) |
+                  ((1u << (prob->tile / pin)) - 1u) << 16;
+    if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
+    return dispatch<kModeRagged>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
 }
 
 extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const void *k,

@@ -18,8 +18,14 @@ struct DebugWaits {
 };
 DebugWaits debug_waits();
 
-// scalar / pointer validation shared by every entry point
+// scalar / pointer validation shared by every entry point of the aligned layout
 sift_status validate_problem(const sift_problem *p, bool attention);
+
+// the same for the general (ragged) layout of sift_decode_ragged and friends
+sift_status validate_ragged(const sift_problem *p, bool attention);
+
+// upper bound on the per-segment query tiles: ceil(tokens/tile) + documents + prompts
+int64_t max_query_tiles(const sift_problem *p);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -15,8 +15,12 @@
  * Readings where the pages are silent (all stated here, applied everywhere):
  *   - bits are kept per KV head (grouped-query attention shares one list per
  *     KV head among its query heads);
- *   - tile size == KV page size == `tile` tokens; every prompt, document and
+ *   - sift_decode / sift_sparse_prefill / sift_fused_prefill / sift_dense_prefill:
+ *     tile size == KV page size == `tile` tokens and every prompt, document and
  *     suffix boundary is a multiple of `tile`;
+ *   - sift_decode_ragged / sift_sparse_prefill_ragged: documents and suffixes
+ *     of any length, each tiled from its own first token (the last tile
+ *     partial), and CA pages of `page` tokens counted the same way;
  *   - diagonal tiles are always computed, causally inside the tile;
  *   - the user-query suffix after the last document attends densely to the
  *     whole prompt;
@@ -66,13 +70,18 @@ typedef enum {
  * [cu_seqlens[p], cu_seqlens[p+1]); it holds documents doc_cu[p] ..
  * doc_cu[p+1]-1, laid out back to back from the prompt start (document g ends
  * at token doc_end[g], exclusive), followed by the user-query suffix up to
- * the prompt end (possibly empty).  Tiles are numbered globally:
- * tile i covers tokens [i*tile, (i+1)*tile); N = total_tokens / tile.
+ * the prompt end (possibly empty).  In the aligned entry points tiles are
+ * numbered globally: tile i covers tokens [i*tile, (i+1)*tile);
+ * N = total_tokens / tile.
  *
- * Bit words (uint64, bit j of a row is bit j%64 of word j/64, LSB first):
- *   LA of document g (T_g tiles, W_g = ceil(T_g/64)) for (layer l, kv head h):
+ * Bit words (uint64, bit j of a row is bit j%64 of word j/64, LSB first), for
+ * a document of n_g tokens with T_g = ceil(n_g/tile) tiles and
+ * C_g = ceil(n_g/page) pages, both counted from its first token:
+ *   LA of document g (W_g = ceil(T_g/64)) for (layer l, kv head h):
  *     T_g rows of W_g words at la_words[la_off[g] + (l*Hkv + h)*T_g*W_g + row*W_g];
- *   CA of document g for (l, h): W_g words at ca_words[ca_off[g] + (l*Hkv + h)*W_g].
+ *   CA of document g for (l, h) (V_g = ceil(C_g/64)): V_g words at
+ *     ca_words[ca_off[g] + (l*Hkv + h)*V_g].
+ * On an aligned layout with page == tile, T_g = C_g = n_g/tile and V_g = W_g.
  */
 typedef struct {
     int32_t num_prompts;           /* P >= 1                                            */
@@ -81,10 +90,14 @@ typedef struct {
     int32_t num_q_heads;           /* Hq                                                */
     int32_t num_kv_heads;          /* Hkv; Hq/Hkv must be even (query heads go in pairs) */
     int32_t head_dim;              /* d: 64 or 128                                      */
-    int32_t tile;                  /* tile = page size in tokens: 64 or 128             */
+    int32_t tile;                  /* LA tile / attention tile in tokens: 64 or 128     */
     int32_t total_tokens;          /* cu_seqlens[P]                                     */
-    int32_t max_tiles_per_prompt;  /* rowcap: capacity of one kv_idx row, >= longest prompt's tiles */
-    int32_t reserved;
+    int32_t max_tiles_per_prompt;  /* rowcap: capacity of one list row, >= the key tiles of
+                                      the longest prompt (ragged: the sum over its segments
+                                      of ceil(length/tile))                             */
+    int32_t page;                  /* CA page size in tokens; 0 = tile.  The aligned entry
+                                      points need 0 or tile; the ragged ones a power of two
+                                      that nests with tile, at most 16 pages per tile   */
     const int32_t *cu_seqlens;     /* device [P+1]                                      */
     const int32_t *doc_cu;         /* device [P+1]                                      */
     const int32_t *doc_end;        /* device [D] (may be NULL when D == 0)              */
@@ -238,6 +251,60 @@ sift_status sift_build_bits(const sift_problem *prob, int32_t layer, const void 
                             float softmax_scale, uint64_t *la_words, uint64_t *ca_words,
                             void *workspace, size_t workspace_bytes, int32_t *dev_status,
                             cudaStream_t stream);
+
+/*
+ * Decode on a general layout: documents and suffixes of any length, CA pages
+ * of their own size.  (SIFT pages, "Dettagli di Implementazione": decoding
+ * kernel; the pages give no tile or page size.)
+ *
+ * Segments are the documents and the query suffixes; each is cut into query
+ * tiles of `tile` tokens from its own first token, the last one partial, and
+ * the tiles of all segments are numbered q = 0 .. num_query_tiles-1 in token
+ * order.  num_query_tiles must equal the sum over segments of
+ * ceil(length/tile) (the host knows the lengths; a mismatch found on the
+ * device is SIFT_ERR_DEVICE_CHECK).
+ *   qtiles  int32 [num_query_tiles][2]: (first token, rows) of each query tile
+ *   kv      int32 [num_layers][Hkv][num_query_tiles][max_tiles_per_prompt][2]:
+ *           row (l, h, q) holds counts[l][h][q] pairs (first token, info) of
+ *           key tiles, by ascending first token: every tile of each earlier
+ *           document of the prompt holding a CA-flagged page, then the
+ *           LA-flagged tiles below the row inside its own document, then the
+ *           row's own tile; a suffix row lists every tile of its prompt's
+ *           documents, its earlier suffix tiles, then its own tile.
+ *           info = len | causal << 8 | mask << 16, Pin = min(page, tile):
+ *             len    keys of the tile inside its segment (1 .. tile);
+ *             causal 1 on the row's own tile only;
+ *             mask   bit k covers keys [k*Pin, (k+1)*Pin) of the tile: the
+ *                    flagged pages of a CA tile, every bit otherwise.
+ *           Key (first + c) is visible to query row r iff c < len, mask bit
+ *           c/Pin is set and, when causal, c <= r.  Entries past the count
+ *           are not written.
+ *   counts  int32 [num_layers][Hkv][num_query_tiles]
+ *   sched   int32 [num_layers][Hkv*num_query_tiles]: per layer, a permutation
+ *           of the units u = h*num_query_tiles + q with non-increasing counts.
+ * Bit-exact for qtiles, kv and counts.  Three kernel launches.
+ */
+sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles,
+                               const uint64_t *la_words, const uint64_t *ca_words,
+                               int32_t *qtiles, int32_t *kv, int32_t *counts, int32_t *sched,
+                               int32_t *dev_status, cudaStream_t stream);
+
+/*
+ * Block-sparse causal grouped-query flash attention of one layer on a general
+ * layout, over sift_decode_ragged's lists: query tile q of query head qh
+ * attends to the visible keys of the entries of row
+ * (layer, qh / (Hq/Hkv), q).  Same q, k, v, o, lse layouts and workspace as
+ * sift_sparse_prefill (total_tokens need not be a multiple of tile); only the
+ * rows of each query tile inside its segment are written.
+ * One memset and one kernel launch.
+ */
+sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int32_t num_query_tiles,
+                                       int32_t layer, const void *q, const void *k,
+                                       const void *v, const int32_t *qtiles, const int32_t *kv,
+                                       const int32_t *counts, const int32_t *sched,
+                                       float softmax_scale, void *o, float *lse,
+                                       void *workspace, size_t workspace_bytes,
+                                       int32_t *dev_status, cudaStream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char *sift_status_string(sift_status status);

@@ -31,13 +31,13 @@ def test_status_strings(lib):
     import bit_vector_guided_gb300 as sift
     for code, name in sift.STATUS.items():
         assert sift.status_string(code) == name
-    assert sift.abi_version() == 100
+    assert sift.abi_version() == 101
 
 
 def _struct(**over):
     from bit_vector_guided_gb300._native import _Problem
     f = dict(num_prompts=1, num_docs=0, num_layers=1, num_q_heads=4, num_kv_heads=2,
-             head_dim=128, tile=128, total_tokens=256, max_tiles_per_prompt=2, reserved=0,
+             head_dim=128, tile=128, total_tokens=256, max_tiles_per_prompt=2, page=0,
              cu_seqlens=16, doc_cu=32, doc_end=None, la_off=None, ca_off=None,
              la_words_len=0, ca_words_len=0)
     f.update(over)
@@ -77,3 +77,38 @@ def test_host_validation_pointers_and_sizes(lib):
     assert lib.sift_decode(None, d, d, d, d, d, d, None) == 1
     assert lib.sift_decode(ctypes.byref(p), d, d, None, d, d, d, None) == 1
     assert lib.sift_workspace_bytes(None) == 0
+
+
+@pytest.mark.parametrize("over,nq,code", [
+    (dict(page=48), 2, 2),                          # page not a power of two
+    (dict(page=4), 2, 2),                           # 32 pages per tile: beyond the mask
+    (dict(tile=96, total_tokens=200), 3, 2),        # tile not a power of two
+    (dict(total_tokens=200), 0, 1),                 # no query tiles
+    (dict(total_tokens=200), 9, 1),                 # more query tiles than the segments hold
+    (dict(head_dim=96, total_tokens=200), 2, 2),    # unsupported head_dim
+    (dict(num_q_heads=6, num_kv_heads=2), 2, 2),    # odd GQA group
+])
+def test_ragged_host_validation(lib, over, nq, code):
+    p = _struct(**over)
+    d = ctypes.c_void_p(256)
+    rc = lib.sift_sparse_prefill_ragged(ctypes.byref(p), nq, 0, d, d, d, d, d, d, d, 0.0, d, d,
+                                        d, 1 << 20, d, None)
+    assert rc == code
+    if code == 2 and "head_dim" not in over and "num_q_heads" not in over:
+        assert lib.sift_decode_ragged(ctypes.byref(p), max(nq, 1), d, d, d, d, d, d, d,
+                                      None) == 2
+
+
+def test_ragged_layout_rules(lib):
+    """A ragged total is fine for the general entry points and for workspace sizing, but
+    not for the aligned ones; a page size other than the tile is general-layout only."""
+    p = _struct(total_tokens=200)
+    assert lib.sift_workspace_bytes(ctypes.byref(p)) > 0
+    d = ctypes.c_void_p(256)
+    assert lib.sift_decode(ctypes.byref(p), d, d, d, d, d, d, None) == 2
+    p = _struct(page=64)
+    assert lib.sift_dense_prefill(ctypes.byref(p), d, d, d, 0.0, d, d, d, 1 << 20, d, None) == 2
+    # misaligned list pointer (entries are 8-byte pairs)
+    p = _struct(total_tokens=200)
+    assert lib.sift_sparse_prefill_ragged(ctypes.byref(p), 2, 0, d, d, d, d, ctypes.c_void_p(260),
+                                          d, d, 0.0, d, d, d, 1 << 20, d, None) == 1

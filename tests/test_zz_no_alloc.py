@@ -70,7 +70,7 @@ def test_noalloc_rejects_problem_beyond_scratch(sift):
     N = 16400  # 8 kv heads x 16,400 query tiles: 1.05 MB of scratch, above the 1 MiB array
     p = _Problem(num_prompts=1, num_docs=0, num_layers=1, num_q_heads=16, num_kv_heads=8,
                  head_dim=128, tile=128, total_tokens=N * 128, max_tiles_per_prompt=N,
-                 reserved=0, cu_seqlens=16, doc_cu=32, doc_end=None, la_off=None, ca_off=None,
+                 page=0, cu_seqlens=16, doc_cu=32, doc_end=None, la_off=None, ca_off=None,
                  la_words_len=0, ca_words_len=0)
     assert lib.sift_workspace_bytes(ctypes.byref(p)) > (1 << 20)
     d = ctypes.c_void_p(256)

@@ -163,6 +163,15 @@ def custom_config(name, prompts, bits, num_layers=1, num_q_heads=4, num_kv_heads
                   bits, description, int(page))
 
 
+def _ragged_lengths(name: str, n: int, lo: int, hi: int, total: int) -> list:
+    """n seeded document lengths drawn from U[lo, hi], rescaled to sum to `total`."""
+    rng = np.random.Generator(np.random.PCG64(seed_for(name, "lengths")))
+    raw = rng.integers(lo, hi + 1, size=n).astype(np.float64)
+    out = [int(x) for x in np.floor(raw * total / raw.sum())]
+    out[-1] += total - sum(out)
+    return out
+
+
 def _batch4(p: float) -> Config:
     tag = f"batch4_p{int(round(p * 100)):03d}"
     return custom_config(
@@ -190,6 +199,14 @@ CONFIGS = {
         num_layers=32, num_q_heads=32, num_kv_heads=8, head_dim=128, tile=128,
         description="Llama-3.1-8B, 16 docs x 2048 + 256 (33024 tokens) x 32 layers, "
                     "per-(layer,head) LA density U[0.05,0.35], CA half of it"),
+    "llama_32k_ragged": custom_config(
+        "llama_32k_ragged", [(_ragged_lengths("llama_32k_ragged", 16, 1024, 3072, 32731), 293)],
+        BitSpec(head_density=(0.05, 0.35), head_ca_ratio=0.0625),
+        num_layers=32, num_q_heads=32, num_kv_heads=8, head_dim=128, tile=128, page=16,
+        description="Llama-3.1-8B, 16 docs of 1024-3072 tokens (seeded, 32731 in all) + 293 "
+                    "(33024 tokens) x 32 layers, CA pages of 16 tokens; per-(layer,head) LA "
+                    "density U[0.05,0.35], CA page density 1/16 of it (about half of it per "
+                    "128-token tile, as in llama_32k)"),
     "qwen3_64k": custom_config(
         "qwen3_64k", [([2048] * 32, 512)],
         BitSpec(la_p=0.15, ca_p=0.08, ca_first_page=True),
