@@ -402,34 +402,42 @@ __device__ bool walk_bits(const AttnParams &p, const WorkItem &it, uint32_t lane
 
 // General layout: clear (to -inf) the columns of a key tile that row `row` may not use.
 // info = len | causal << 8 | mask << 16: columns c < len whose page bit c >> lp is set,
-// and c <= row on the diagonal.  Built as one 32-bit visibility word per 32 columns.
+// and c <= row on the diagonal.  One 32-column visibility word at a time; words that
+// are wholly visible (most of them) skip the selects.
+__device__ __forceinline__ uint32_t page_word(uint32_t pm, int w, int lp) {
+    if (lp >= 5) return ((pm >> ((32 * w) >> lp)) & 1u) ? kFull : 0u;  // one page per word
+    if (lp == 4) {  // 2 pages of 16 columns: bit k -> bits [16k, 16k+16)
+        const uint32_t b = (pm >> (2 * w)) & 0x3u;
+        return ((b * 0x8001u) & 0x10001u) * 0xffffu;
+    }
+    if (lp == 3) {  // 4 pages of 8 columns: bit k -> byte k
+        const uint32_t b = (pm >> (4 * w)) & 0xfu;
+        return ((b * 0x00204081u) & 0x01010101u) * 0xffu;
+    }
+    uint32_t out = 0u;  // lp == 2: 8 pages of 4 columns (64-token tiles only)
+    const uint32_t b = (pm >> (8 * w)) & 0xffu;
+    for (int k = 0; k < 8; ++k)
+        if ((b >> k) & 1u) out |= 0xfu << (4 * k);
+    return out;
+}
+
 template <int BT>
 __device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int row, int lp) {
     const int len = static_cast<int>(info & 0xffu);
     const bool causal = (info >> 8) & 1u;
     const uint32_t pm = info >> 16;
-    uint32_t vis[BT / 32];
 #pragma unroll
     for (int w = 0; w < BT / 32; ++w) {
         const int c0 = 32 * w;
-        const uint32_t lm = len >= c0 + 32 ? kFull : (len <= c0 ? 0u : (1u << (len - c0)) - 1u);
-        uint32_t pw;
-        if (lp >= 5) {
-            pw = ((pm >> (c0 >> lp)) & 1u) ? kFull : 0u;
-        } else {
-            const int per = 32 >> lp;
-            const uint32_t ones = (1u << (1 << lp)) - 1u;
-            pw = 0u;
-            for (int k = 0; k < per; ++k)
-                if ((pm >> (w * per + k)) & 1u) pw |= ones << (k << lp);
-        }
-        uint32_t cm = kFull;
-        if (causal) cm = row >= c0 + 31 ? kFull : (row < c0 ? 0u : (2u << (row - c0)) - 1u);
-        vis[w] = lm & pw & cm;
-    }
+        uint32_t vis = len >= c0 + 32 ? kFull : (len <= c0 ? 0u : (1u << (len - c0)) - 1u);
+        vis &= page_word(pm, w, lp);
+        if (causal) vis &= row >= c0 + 31 ? kFull : (row < c0 ? 0u : (2u << (row - c0)) - 1u);
+        if (vis != kFull) {
 #pragma unroll
-    for (int c = 0; c < BT; ++c)
-        if (!((vis[c >> 5] >> (c & 31)) & 1u)) x[c] = -INFINITY;
+            for (int t = 0; t < 32; ++t)
+                if (!((vis >> t) & 1u)) x[c0 + t] = -INFINITY;
+        }
+    }
 }
 
 template <int BT, int HD, int MODE>

@@ -37,7 +37,7 @@ _lib = None
 
 __all__ = ["build", "load", "decode", "schedule", "attention_rows", "attention_all",
            "key_mask", "brute_force_attention", "tile_mask", "set_threads", "decode_ragged",
-           "token_mask",
+           "token_mask", "page_capacity",
            "doc_tile_masses", "top_count", "select_top", "build_bits"]
 
 
@@ -66,7 +66,7 @@ def load():
         lib.sift_oracle_decode.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P, i32, P, P]
         lib.sift_oracle_decode.restype = i32
         lib.sift_oracle_decode_ragged.argtypes = [i32, i32, i32, i32, i32, i32, P, P, P, P, P,
-                                                  P, P, i32, i32, P, P, P]
+                                                  P, P, i32, i32, i32, P, P, P, P]
         lib.sift_oracle_decode_ragged.restype = i32
         lib.sift_oracle_attention_rows.argtypes = [i32, i32, i32, i32, i32, P, P, P, P, P, P, P,
                                                    i32, i32, i32, f64, P, P, P, i64, P, P, P, P]
@@ -128,26 +128,37 @@ def decode(layout, la_words, ca_words, rowcap: Optional[int] = None):
     return kv_idx, counts
 
 
-def decode_ragged(layout, la_words, ca_words, rowcap: Optional[int] = None):
+def page_capacity(layout) -> int:
+    """Gathered pages per (layer, kv head, document): rowcap x pages per tile when pages
+    are gathered (page < tile, a multiple of 8), else 0."""
+    P, B = _page(layout), int(layout.tile)
+    return int(layout.max_tiles_per_prompt) * (B // P) if (P < B and P % 8 == 0) else 0
+
+
+def decode_ragged(layout, la_words, ca_words, rowcap: Optional[int] = None,
+                  page_cap: Optional[int] = None):
     """Per-segment query tiles and their (first token, info) key-tile lists, for documents
     of any length and a CA page size of its own (rule in sift_oracle.c).
 
     Returns (qtiles int32 [NQ, 2], kv int32 [L, Hkv, NQ, rowcap, 2] with -1 padding,
-    counts int32 [L, Hkv, NQ]).
+    counts int32 [L, Hkv, NQ], pages int32 [L, Hkv, D, page_cap] with -1 padding).
     """
     lib = load()
     rowcap = rowcap or layout.max_tiles_per_prompt
-    L, Hkv, NQ = layout.num_layers, layout.num_kv_heads, layout.num_query_tiles
+    page_cap = page_capacity(layout) if page_cap is None else int(page_cap)
+    L, Hkv, NQ, D = layout.num_layers, layout.num_kv_heads, layout.num_query_tiles, layout.num_docs
     qtiles = np.zeros((max(NQ, 1), 2), np.int32)
     kv = np.full((L, Hkv, max(NQ, 1), rowcap, 2), -1, np.int32)
     counts = np.zeros((L, Hkv, max(NQ, 1)), np.int32)
+    pages = np.full((L, Hkv, max(D, 1), max(page_cap, 1)), -1, np.int32)
     arrs = _layout_args(layout, la_words, ca_words)
     rc = lib.sift_oracle_decode_ragged(layout.num_prompts, layout.num_docs, L, Hkv, layout.tile,
                                        _page(layout), *[_ptr(a) for a in arrs], NQ, rowcap,
-                                       _ptr(qtiles), _ptr(kv), _ptr(counts))
+                                       page_cap, _ptr(qtiles), _ptr(kv), _ptr(counts),
+                                       _ptr(pages))
     if rc != 0:
-        raise ValueError("oracle ragged decode: bad page size, tile count or row capacity")
-    return qtiles[:NQ], kv[:, :, :NQ], counts[:, :, :NQ]
+        raise ValueError("oracle ragged decode: bad page size, tile count or capacity")
+    return qtiles[:NQ], kv[:, :, :NQ], counts[:, :, :NQ], pages[:, :, :D, :page_cap]
 
 
 def schedule(counts: np.ndarray) -> np.ndarray:

@@ -208,7 +208,7 @@ int sift_oracle_decode(int num_prompts, int num_docs, int num_layers, int num_kv
  *     row's own document, then the diagonal tile;
  *   - a suffix row: every tile of every document of the prompt, the suffix's
  *     own tiles before the diagonal, then the diagonal.
- * info = len | causal << 8 | mask << 16, with Pin = min(page, tile):
+ * info = len | causal << 8 | gather << 9 | mask << 16, with Pin = min(page, tile):
  *   len     keys of the tile inside its segment (1 .. tile);
  *   causal  1 on the diagonal only;
  *   mask    bit k covers keys [k*Pin, (k+1)*Pin) of the tile; all tile/Pin
@@ -216,15 +216,31 @@ int sift_oracle_decode(int num_prompts, int num_docs, int num_layers, int num_kv
  *           the page holding key k*Pin (0 when k*Pin >= len).
  * Key (first + c) of an entry is visible to row r of the query tile iff
  * c < len, mask bit c / Pin is set, and c <= r when causal -- the same key
- * set as key_visible().  kv holds rowcap pairs per row, row (l*Hkv + h)*nq + q.
- * Returns 0, or -1 if the segments do not make nq tiles or a row exceeds rowcap.
+ * set as key_visible().
+ *
+ * Gathered pages (page < tile and page a multiple of 8): a document row's
+ * CA part is instead made of pages, not tiles.  The whole flagged pages of
+ * the earlier documents (page j of a document with (j+1)*page <= its length),
+ * in ascending order, are written to pages[((l*Hkv + h)*D + g)*page_cap + k]
+ * (first token of the k-th) for the row's document g, and listed tile/page at
+ * a time: entry (first = (h*D + g)*page_cap + k0, info = n*page | 1 << 9 |
+ * all mask bits) stands for the n <= tile/page pages k0 .. k0+n-1, laid side
+ * by side (key c is token pages[.. + k0 + c/page] + c%page).  After these
+ * groups comes each earlier document's last page when it is partial and
+ * flagged, as an ordinary entry (its first token, len = length % page, mask
+ * bit 0).  The rest of the row is as above.
+ *
+ * kv holds rowcap pairs per row, row (l*Hkv + h)*nq + q.  Returns 0, or -1
+ * if the segments do not make nq tiles, a row exceeds rowcap or a document's
+ * pages exceed page_cap.
  */
 int sift_oracle_decode_ragged(int num_prompts, int num_docs, int num_layers, int num_kv_heads,
                               int tile, int page, const int32_t *cu_seqlens,
                               const int32_t *doc_cu, const int32_t *doc_end,
                               const int64_t *la_off, const int64_t *ca_off,
                               const uint64_t *la_words, const uint64_t *ca_words, int nq,
-                              int rowcap, int32_t *qtiles, int32_t *kv, int32_t *counts) {
+                              int rowcap, int page_cap, int32_t *qtiles, int32_t *kv,
+                              int32_t *counts, int32_t *pages) {
     sift_bits_view s = {num_prompts, num_docs, num_kv_heads, tile, page, cu_seqlens, doc_cu,
                         doc_end, la_off, ca_off, la_words, ca_words};
     if (tile < 1 || page < 1 || (page < tile ? tile % page : page % tile) != 0 ||
@@ -233,6 +249,7 @@ int sift_oracle_decode_ragged(int num_prompts, int num_docs, int num_layers, int
     const int pin = page < tile ? page : tile;
     const int nbits = tile / pin;
     const uint32_t full = (1u << nbits) - 1u;
+    const int gather = page < tile && page % 8 == 0;
     int bad = 0;
     int q = 0;
     for (int p = 0; p < num_prompts; ++p)
@@ -264,7 +281,31 @@ int sift_oracle_decode_ragged(int num_prompts, int num_docs, int num_layers, int
                         int n = 0;
 #define EMIT(first, info) do { if (n < rowcap) { out[2 * n] = (int32_t)(first); \
                                out[2 * n + 1] = (int32_t)(info); } else bad = 1; ++n; } while (0)
-                        for (int gp = doc_cu[p]; gp < g; ++gp) {
+                        if (!suffix && gather) {
+                            int64_t pbase = (((int64_t)l * num_kv_heads + h) * num_docs + g) * page_cap;
+                            int64_t rel = ((int64_t)h * num_docs + g) * page_cap;
+                            int npg = 0;
+                            for (int gp = doc_cu[p]; gp < g; ++gp) {
+                                int64_t ds = doc_begin(&s, p, gp), de = doc_end[gp];
+                                for (int j = 0; (int64_t)(j + 1) * page <= de - ds; ++j)
+                                    if (ca_bit(&s, p, gp, l, h, j)) {
+                                        if (npg < page_cap) pages[pbase + npg] = (int32_t)(ds + (int64_t)j * page);
+                                        else bad = 1;
+                                        ++npg;
+                                    }
+                            }
+                            for (int k0 = 0; k0 < npg; k0 += nbits) {
+                                int in_group = npg - k0 < nbits ? npg - k0 : nbits;
+                                EMIT(rel + k0, (uint32_t)(in_group * page) | 1u << 9 | full << 16);
+                            }
+                            for (int gp = doc_cu[p]; gp < g; ++gp) {
+                                int64_t ds = doc_begin(&s, p, gp), de = doc_end[gp];
+                                int64_t rem = (de - ds) % page;
+                                if (rem && ca_bit(&s, p, gp, l, h, (int)((de - ds) / page)))
+                                    EMIT(de - rem, (uint32_t)rem | 1u << 16);
+                            }
+                        }
+                        for (int gp = doc_cu[p]; gp < g && !(!suffix && gather); ++gp) {
                             int64_t ds = doc_begin(&s, p, gp), de = doc_end[gp];
                             for (int64_t y = ds; y < de; y += tile) {
                                 int64_t len = de - y < tile ? de - y : tile;

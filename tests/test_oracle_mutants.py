@@ -55,6 +55,10 @@ MUTANTS = [
      "if (ca_bit(&s, p, gp, l, h, (int)((y - ds) / page)))"),
     ("ragged_full_length_tiles", "int64_t len = de - y < tile ? de - y : tile;",
      "int64_t len = tile;"),
+    ("gather_takes_partial_pages", "for (int j = 0; (int64_t)(j + 1) * page <= de - ds; ++j)",
+     "for (int j = 0; (int64_t)j * page < de - ds; ++j)"),
+    ("gather_groups_always_full", "EMIT(rel + k0, (uint32_t)(in_group * page) | 1u << 9 | full << 16);",
+     "EMIT(rel + k0, (uint32_t)(nbits * page) | 1u << 9 | full << 16);"),
     ("ragged_diagonal_not_causal",
      "EMIT(x, (uint32_t)(end - x < tile ? end - x : tile) | 1u << 8 | full << 16);",
      "EMIT(x, (uint32_t)(end - x < tile ? end - x : tile) | full << 16);"),

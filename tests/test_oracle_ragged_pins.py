@@ -42,13 +42,16 @@ def _golden():
     return g, lay, np.array(g["la_words"], np.uint64), np.array(g["ca_words"], np.uint64)
 
 
-def expand_lists(lay, qtiles, kv, counts, layer, h):
-    """Token mask implied by the decoded lists: key (first + c) is visible to row r of
-    the query tile iff c < len, mask bit c // Pin is set and, when causal, c <= r."""
-    T, B = lay.total_tokens, lay.tile
-    pin = min(lay.page_size, B)
+def expand_lists(lay, qtiles, kv, counts, pages, layer, h):
+    """Token mask implied by the decoded lists: key c of an entry is visible to row r of
+    the query tile iff c < len, mask bit c // Pin is set and, when causal, c <= r.  Key c
+    is token first + c, or, for a gathered entry, token pages[first + c // page] + c % page
+    of the layer's page array."""
+    T, B, P = lay.total_tokens, lay.tile, lay.page_size
+    pin = min(P, B)
     M = np.zeros((T, T), bool)
     c = np.arange(B)
+    flat = pages[layer].reshape(-1)
     for q, (x, rows) in enumerate(qtiles):
         r = np.arange(rows)
         for e in range(counts[layer, h, q]):
@@ -59,13 +62,17 @@ def expand_lists(lay, qtiles, kv, counts, layer, h):
             if causal:
                 vis &= c[None, :] <= r[:, None]
             rr, cc = np.nonzero(vis)
-            M[x + rr, first + cc] = True
+            if (info >> 9) & 1:
+                keys = flat[first + cc // P] + cc % P
+            else:
+                keys = first + cc
+            M[x + rr, keys] = True
     return M
 
 
 def test_ragged_golden_fixture():
     g, lay, la, ca = _golden()
-    qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
+    qt, kv, cnt, pg = oracle.decode_ragged(lay, la, ca)
     assert qt.tolist() == g["expected_qtiles"]
     for q, row in enumerate(g["expected_rows"]):
         assert cnt[0, 0, q] == len(row), q
@@ -73,7 +80,34 @@ def test_ragged_golden_fixture():
     # and the fixture's lists are the key set of the token rule
     T = lay.total_tokens
     tok = np.arange(T)
-    assert np.array_equal(expand_lists(lay, qt, kv, cnt, 0, 0),
+    assert np.array_equal(expand_lists(lay, qt, kv, cnt, pg, 0, 0),
+                          oracle.key_mask(lay, la, ca, 0, 0, tok, tok))
+
+
+def _golden_gather():
+    with open(os.path.join(GOLDEN, "decode_gather_small.json")) as f:
+        g = json.load(f)
+    lay = W.Layout(num_prompts=1, num_docs=3, num_layers=1, num_q_heads=2, num_kv_heads=1,
+                   head_dim=8, tile=g["tile"], total_tokens=g["cu_seqlens"][-1],
+                   max_tiles_per_prompt=6, cu_seqlens=np.array(g["cu_seqlens"], np.int32),
+                   doc_cu=np.array(g["doc_cu"], np.int32),
+                   doc_end=np.array(g["doc_end"], np.int32),
+                   la_off=np.array(g["la_off"], np.int64), ca_off=np.array(g["ca_off"], np.int64),
+                   la_words_len=len(g["la_words"]), ca_words_len=len(g["ca_words"]),
+                   page=g["page"])
+    return g, lay, np.array(g["la_words"], np.uint64), np.array(g["ca_words"], np.uint64)
+
+
+def test_gathered_pages_golden_fixture():
+    g, lay, la, ca = _golden_gather()
+    qt, kv, cnt, pg = oracle.decode_ragged(lay, la, ca, page_cap=g["page_cap"])
+    assert qt.tolist() == g["expected_qtiles"]
+    for q, row in enumerate(g["expected_rows"]):
+        assert cnt[0, 0, q] == len(row), q
+        assert kv[0, 0, q, :len(row)].tolist() == row, q
+    assert pg[0, 0].tolist() == g["expected_pages"]
+    tok = np.arange(lay.total_tokens)
+    assert np.array_equal(expand_lists(lay, qt, kv, cnt, pg, 0, 0),
                           oracle.key_mask(lay, la, ca, 0, 0, tok, tok))
 
 
@@ -107,7 +141,7 @@ def test_ragged_lists_token_rule_and_numpy_mask_agree(cfg):
     lay = W.make_layout(cfg)
     la, ca = W.make_bits(cfg, lay)
     assert not lay.aligned or cfg.name == "rg_eq"
-    qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
+    qt, kv, cnt, pg = oracle.decode_ragged(lay, la, ca)
     T, B = lay.total_tokens, lay.tile
     tok = np.arange(T)
     # query tiles: every segment cut from its own start, in token order
@@ -117,14 +151,16 @@ def test_ragged_lists_token_rule_and_numpy_mask_agree(cfg):
     assert qt.tolist() == exp
     for l in range(lay.num_layers):
         for h in range(lay.num_kv_heads):
-            A = expand_lists(lay, qt, kv, cnt, l, h)
+            A = expand_lists(lay, qt, kv, cnt, pg, l, h)
             Bm = oracle.key_mask(lay, la, ca, l, h, tok, tok)
             C = oracle.token_mask(lay, la, ca, l, h)
             assert np.array_equal(A, Bm), (l, h)
             assert np.array_equal(Bm, C), (l, h)
             for q, (x, rows) in enumerate(qt):
-                firsts = kv[l, h, q, :cnt[l, h, q], 0]
-                assert np.all(np.diff(firsts) > 0), "lists ascend by first token"
+                ent = kv[l, h, q, :cnt[l, h, q]]
+                plain = ent[(ent[:, 1] >> 9) & 1 == 0, 0]
+                assert np.all(np.diff(plain[:-1]) > 0) if len(plain) > 2 else True
+                firsts = ent[:, 0]
                 assert firsts[-1] == x and (kv[l, h, q, cnt[l, h, q] - 1, 1] >> 8) & 1 == 1
                 assert np.all((kv[l, h, q, :cnt[l, h, q] - 1, 1] >> 8) & 1 == 0)
 
@@ -150,7 +186,7 @@ def test_ragged_decode_reduces_to_aligned_decode(name):
     assert lay.aligned
     la, ca = W.make_bits(cfg, lay)
     kv_a, cnt_a = oracle.decode(lay, la, ca)
-    qt, kv_r, cnt_r = oracle.decode_ragged(lay, la, ca)
+    qt, kv_r, cnt_r, _ = oracle.decode_ragged(lay, la, ca)
     B = lay.tile
     assert qt.tolist() == [[i * B, B] for i in range(lay.num_tiles)]
     assert np.array_equal(cnt_a, cnt_r)
@@ -164,7 +200,7 @@ def test_ragged_decode_reduces_to_aligned_decode(name):
                 assert np.all(info[:-1] == full) and info[-1] == full | (1 << 8)
 
 
-@pytest.mark.parametrize("page,tile", [(32, 8), (4, 16), (8, 8), (2, 16)])
+@pytest.mark.parametrize("page,tile", [(32, 8), (4, 16), (8, 8), (2, 16), (8, 16), (16, 64)])
 def test_single_ca_bit_covers_exactly_its_page(page, tile):
     """One CA bit of the first document admits exactly the keys of its page -- tokens
     [j*page, (j+1)*page) of that document, cut at the document's end -- to every query
@@ -183,8 +219,8 @@ def test_single_ca_bit_covers_exactly_its_page(page, tile):
         want = np.zeros(n0, bool)
         want[j * page: min((j + 1) * page, n0)] = True
         assert np.all(M == want[None, :]), (page, tile, j)
-        qt, kv, cnt = oracle.decode_ragged(lay, la, ca)
-        A = expand_lists(lay, qt, kv, cnt, 0, 0)
+        qt, kv, cnt, pg = oracle.decode_ragged(lay, la, ca)
+        A = expand_lists(lay, qt, kv, cnt, pg, 0, 0)
         assert np.array_equal(A[n0:, :n0], np.broadcast_to(want, (len(q), n0)))
 
 
