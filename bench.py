@@ -632,18 +632,21 @@ def run_ragged(args, dev, stream):
     kv = torch.empty((L, H, NQ, R, 2), dtype=torch.int32, device=dev)
     cnt = torch.empty((L, H, NQ), dtype=torch.int32, device=dev)
     sch = torch.empty((L, H * NQ), dtype=torch.int32, device=dev)
+    pages = (torch.empty((L, H, lay.num_docs, prob.page_cap), dtype=torch.int32, device=dev)
+             if prob.page_cap > 0 else None)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(L + 2)]
 
     def step(record=False):
         if record:
             ev[0].record(stream)
-        sift.decode_ragged(prob, la_d, ca_d, qt, kv, cnt, sch, dev_status=st, stream=stream)
+        sift.decode_ragged(prob, la_d, ca_d, qt, kv, cnt, sch, pages, dev_status=st,
+                           stream=stream)
         if record:
             ev[1].record(stream)
         for l in range(L):
             q, k, v = qkv[l]
-            sift.sparse_prefill_ragged(prob, l, q, k, v, qt, kv, cnt, sch, 0.0, o, lse, ws, st,
-                                       stream)
+            sift.sparse_prefill_ragged(prob, l, q, k, v, qt, kv, cnt, sch, pages, 0.0, o, lse,
+                                       ws, st, stream)
             if record:
                 ev[2 + l].record(stream)
 

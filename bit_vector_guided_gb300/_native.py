@@ -75,10 +75,10 @@ def load_library(path: Optional[str] = None):
     lib.sift_build_bits_workspace_bytes.restype = sz
     lib.sift_build_bits.argtypes = [P, i32, P, P, i32, f32, f32, f32, P, P, P, sz, P, P]
     lib.sift_build_bits.restype = i32
-    lib.sift_decode_ragged.argtypes = [P, i32, P, P, P, P, P, P, P, P]
+    lib.sift_decode_ragged.argtypes = [P, i32, P, P, P, P, P, P, P, i32, P, P]
     lib.sift_decode_ragged.restype = i32
-    lib.sift_sparse_prefill_ragged.argtypes = [P, i32, i32, P, P, P, P, P, P, P, f32, P, P, P,
-                                               sz, P, P]
+    lib.sift_sparse_prefill_ragged.argtypes = [P, i32, i32, P, P, P, P, P, P, P, P, i32, f32,
+                                               P, P, P, sz, P, P]
     lib.sift_sparse_prefill_ragged.restype = i32
     lib.sift_status_string.argtypes = [i32]
     lib.sift_status_string.restype = ctypes.c_char_p
@@ -162,6 +162,9 @@ class SiftProblem:
         if max_tiles_per_prompt is None:
             max_tiles_per_prompt = int(np.max(np.diff(cu)) // self.tile) if len(cu) > 1 else 1
         self.max_tiles_per_prompt = max(int(max_tiles_per_prompt), 1)
+        # gathered CA pages (page below the tile, a multiple of 8): capacity per document
+        pg = self.page if self.page > 0 else B
+        self.page_cap = self.max_tiles_per_prompt * (B // pg) if (pg < B and pg % 8 == 0) else 0
         self.device = torch.device(device)
 
         def up(a, dt):
@@ -354,9 +357,10 @@ def build_bits(prob: SiftProblem, layer: int, q, k, max_doc_tiles: int, la_fract
 
 
 def decode_ragged(prob: SiftProblem, la_words, ca_words, qtiles=None, kv=None, counts=None,
-                  sched=None, dev_status=None, stream=None):
+                  sched=None, pages=None, dev_status=None, stream=None):
     """sift_decode_ragged: returns (qtiles [NQ,2], kv [L,Hkv,NQ,rowcap,2], counts [L,Hkv,NQ],
-    sched [L,Hkv*NQ]) for documents of any length and a CA page size of their own."""
+    sched [L,Hkv*NQ], pages [L,Hkv,D,page_cap] or None) for documents of any length and a
+    CA page size of their own."""
     import torch
     lib = load_library()
     L, H, NQ, R = prob.num_layers, prob.num_kv_heads, prob.num_query_tiles, prob.max_tiles_per_prompt
@@ -369,18 +373,21 @@ def decode_ragged(prob: SiftProblem, la_words, ca_words, qtiles=None, kv=None, c
         counts = torch.empty((L, H, NQ), dtype=torch.int32, device=dev)
     if sched is None:
         sched = torch.empty((L, H * NQ), dtype=torch.int32, device=dev)
+    if pages is None and prob.page_cap > 0 and prob.num_docs > 0:
+        pages = torch.empty((L, H, prob.num_docs, prob.page_cap), dtype=torch.int32, device=dev)
     if dev_status is None:
         dev_status = prob.new_status()
     rc = lib.sift_decode_ragged(prob.ref, NQ, _ptr(la_words), _ptr(ca_words), _ptr(qtiles),
-                                _ptr(kv), _ptr(counts), _ptr(sched), _ptr(dev_status),
+                                _ptr(kv), _ptr(counts), _ptr(sched), _ptr(pages),
+                                prob.page_cap if pages is not None else 0, _ptr(dev_status),
                                 _stream(stream))
     _check(rc, "sift_decode_ragged")
-    return qtiles, kv, counts, sched
+    return qtiles, kv, counts, sched, pages
 
 
 def sparse_prefill_ragged(prob: SiftProblem, layer: int, q, k, v, qtiles, kv, counts, sched,
-                          softmax_scale: float = 0.0, o=None, lse=None, workspace=None,
-                          dev_status=None, stream=None):
+                          pages=None, softmax_scale: float = 0.0, o=None, lse=None,
+                          workspace=None, dev_status=None, stream=None):
     """sift_sparse_prefill_ragged: returns (o bf16 [T,Hq,d], lse fp32 [Hq,T])."""
     import torch
     lib = load_library()
@@ -395,7 +402,9 @@ def sparse_prefill_ragged(prob: SiftProblem, layer: int, q, k, v, qtiles, kv, co
         dev_status = prob.new_status()
     rc = lib.sift_sparse_prefill_ragged(prob.ref, prob.num_query_tiles, int(layer), _ptr(q),
                                         _ptr(k), _ptr(v), _ptr(qtiles), _ptr(kv), _ptr(counts),
-                                        _ptr(sched), float(softmax_scale), _ptr(o), _ptr(lse),
+                                        _ptr(sched), _ptr(pages),
+                                        prob.page_cap if pages is not None else 0,
+                                        float(softmax_scale), _ptr(o), _ptr(lse),
                                         _ptr(workspace), int(workspace.numel()), _ptr(dev_status),
                                         _stream(stream))
     _check(rc, "sift_sparse_prefill_ragged")

@@ -116,7 +116,12 @@ struct AttnParams {
     const int32_t *qt;       // [NQ][2] (first token, rows)
     int32_t lp;              // log2 of min(page, tile)
     uint32_t full_info;      // info of a whole tile with every page kept
+    const int32_t *pages;    // gathered pages: layer slice [Hkv][D][page_cap] of first tokens
+    int64_t pages_len;       // entries in that slice
+    int32_t page;            // page size in tokens (gathered loads are page rows high)
 };
+
+constexpr uint32_t kGatherBit = 1u << 9;  // list entry of gathered pages (general layout)
 
 template <int BT, int HD>
 struct Geo {
@@ -221,20 +226,35 @@ __device__ __forceinline__ int list_entry(const AttnParams &p, const WorkItem &i
     constexpr bool DENSE = MODE == kModeDense;
     if (j >= it.n) return 0;
     if (DENSE) return it.first + j;
-    if constexpr (MODE == kModeRagged) {  // the key tile's first token
-        int x = __ldg(&p.kv2[it.list + j].x);
-        if (x < 0 || x > it.q0 || (j == it.n - 1 && x != it.q0)) {
-            set_status(p.status, SIFT_ERR_DEVICE_CHECK);
-            x = it.q0;
-        }
-        return x;
-    }
     int idx = __ldg(p.kv_idx + it.list + j);
     if (idx < 0 || idx > it.i || (j == it.n - 1 && idx != it.i)) {
         set_status(p.status, SIFT_ERR_DEVICE_CHECK);
         idx = it.i;
     }
     return idx;
+}
+
+// general layout: entry j of the item's list as (first, info); a gathered entry's first
+// field is an index into the layer's page array.  Bad entries are reported and replaced
+// by the item's own tile.
+__device__ __forceinline__ int2 ragged_entry(const AttnParams &p, const WorkItem &it, int j) {
+    if (j >= it.n) return make_int2(0, 0);
+    int2 e = __ldg(&p.kv2[it.list + j]);
+    const uint32_t info = static_cast<uint32_t>(e.y);
+    bool ok;
+    if (info & kGatherBit) {
+        const int len = static_cast<int>(info & 0xffu);
+        const int np = len / p.page;
+        ok = j != it.n - 1 && len % p.page == 0 && np >= 1 && np * p.page <= p.B && e.x >= 0 &&
+             e.x <= p.pages_len - np;
+    } else {
+        ok = e.x >= 0 && e.x <= it.q0 && (j != it.n - 1 || e.x == it.q0);
+    }
+    if (!ok) {
+        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+        e = make_int2(it.q0, 0);
+    }
+    return e;
 }
 
 // ---- rows walked from the bits ------------------------------------------------------
@@ -444,7 +464,9 @@ template <int BT, int HD, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
 sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV, const AttnParams p) {
+                      const __grid_constant__ CUtensorMap tmV,
+                      const __grid_constant__ CUtensorMap tmKp,  // page-high boxes (gather)
+                      const __grid_constant__ CUtensorMap tmVp, const AttnParams p) {
     using G = Geo<BT, HD>;
     constexpr bool DENSE = MODE == kModeDense;
     constexpr bool RAGGED = MODE == kModeRagged;  // list entries are first tokens, not tiles
@@ -505,6 +527,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         ptx::prefetch_tmap(&tmQ);
         ptx::prefetch_tmap(&tmK);
         ptx::prefetch_tmap(&tmV);
+        if (RAGGED) {
+            ptx::prefetch_tmap(&tmKp);
+            ptx::prefetch_tmap(&tmVp);
+        }
     }
     if (warp == kMmaWarp) {
         ptx::tmem_alloc(ptx::smem_u32(&c.tmem_base), kTmemCols);
@@ -560,8 +586,46 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 ++kf;
                 return true;
             };
+            // gathered pages: one page-high box per page into consecutive slots of the ring
+            // slot (unused slots take the group's first page again, masked out later)
+            auto load_k_pages = [&](int first, uint32_t info) -> bool {
+                const int np = static_cast<int>(info & 0xffu) / p.page;
+                int ps = 0;
+                if (static_cast<int>(lane) < np) {
+                    ps = __ldg(p.pages + first + lane);
+                    if (ps < 0 || ps > it.q0) {
+                        set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+                        ps = it.q0;
+                    }
+                }
+                const int ks = kf % kKSlots;
+                if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
+                const int per = BT / p.page;
+                for (int sl = 0; sl < per; ++sl) {
+                    const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
+                    if (lane == 0)
+                        for (int b = 0; b < G::kBoxes; ++b)
+                            ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox +
+                                                      sl * p.page * 128,
+                                                  &tmKp, B_(c.k_full[ks]), 64 * b, it.h, pst,
+                                                  pol_kv);
+                }
+                ++kf;
+                return true;
+            };
             if constexpr (MODE == kModeBits) {
                 alive = walk_bits(p, it, lane, load_k);
+            } else if constexpr (RAGGED) {
+                for (int jb = 0; jb < it.n && alive; jb += 32) {
+                    const int2 e = ragged_entry(p, it, jb + static_cast<int>(lane));
+                    const int cnt = min(32, it.n - jb);
+                    for (int jj = 0; jj < cnt && alive; ++jj) {
+                        const int x = __shfl_sync(kFull, e.x, jj);
+                        const uint32_t info = __shfl_sync(kFull, static_cast<uint32_t>(e.y), jj);
+                        alive = (info & kGatherBit) ? load_k_pages(x, info) : load_k(x);
+                    }
+                }
             } else {
                 for (int jb = 0; jb < it.n && alive; jb += 32) {
                     const int idx_l = list_entry<MODE>(p, it, jb + static_cast<int>(lane));
@@ -616,8 +680,41 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 ++vf;
                 return true;
             };
+            auto load_v_pages = [&](int first, uint32_t info) -> bool {
+                const int np = static_cast<int>(info & 0xffu) / p.page;
+                int ps = 0;
+                if (static_cast<int>(lane) < np) {
+                    ps = __ldg(p.pages + first + lane);
+                    if (ps < 0 || ps > it.q0) ps = it.q0;  // reported by the K producer
+                }
+                const int vs = vf % kVSlots;
+                if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) return false;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
+                const int per = BT / p.page;
+                for (int sl = 0; sl < per; ++sl) {
+                    const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
+                    if (lane == 0)
+                        for (int b = 0; b < G::kBoxes; ++b)
+                            ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox +
+                                                      sl * p.page * 128,
+                                                  &tmVp, B_(c.v_full[vs]), 64 * b, it.h, pst,
+                                                  pol_kv);
+                }
+                ++vf;
+                return true;
+            };
             if constexpr (MODE == kModeBits) {
                 alive = walk_bits(p, it, lane, load_v);
+            } else if constexpr (RAGGED) {
+                for (int jb = 0; jb < it.n && alive; jb += 32) {
+                    const int2 e = ragged_entry(p, it, jb + static_cast<int>(lane));
+                    const int cnt = min(32, it.n - jb);
+                    for (int jj = 0; jj < cnt && alive; ++jj) {
+                        const int x = __shfl_sync(kFull, e.x, jj);
+                        const uint32_t info = __shfl_sync(kFull, static_cast<uint32_t>(e.y), jj);
+                        alive = (info & kGatherBit) ? load_v_pages(x, info) : load_v(x);
+                    }
+                }
             } else {
                 for (int jb = 0; jb < it.n && alive; jb += 32) {
                     const int idx_l = list_entry<MODE>(p, it, jb + static_cast<int>(lane));
@@ -777,7 +874,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     float x[BT];
                     if constexpr (BT == 128) ptx::tmem_ld128(tS, x); else ptx::tmem_ld64(tS, x);
                     if constexpr (RAGGED) {
-                        if (info != p.full_info) mask_columns<BT>(x, info, row, p.lp);
+                        if ((info & ~kGatherBit) != p.full_info) mask_columns<BT>(x, info, row, p.lp);
                     } else if (j == it.n - 1) {
 #pragma unroll
                         for (int cidx = 0; cidx < BT; ++cidx)
@@ -920,7 +1017,8 @@ bool make_map(CUtensorMap *m, const void *base, int d, int heads, int tokens, in
 
 template <int BT, int HD, int MODE>
 sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                             const AttnParams &p, cudaStream_t stream) {
+                             const CUtensorMap &mkp, const CUtensorMap &mvp, const AttnParams &p,
+                             cudaStream_t stream) {
     using G = Geo<BT, HD>;
     auto kern = sift_attention_kernel<BT, HD, MODE>;
     static std::once_flag once;
@@ -934,17 +1032,23 @@ sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const
     if (sms <= 0) return SIFT_ERR_CUDA;
     const int grid = p.total_items < sms ? p.total_items : sms;
     if (grid <= 0) return SIFT_OK;
-    kern<<<grid, kThreads, G::kSmem, stream>>>(mq, mk, mv, p);
+    kern<<<grid, kThreads, G::kSmem, stream>>>(mq, mk, mv, mkp, mvp, p);
     return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
 }
 
+// maps: Q, K, V with tile-high boxes, then K, V with page-high boxes (gathered pages of
+// the general layout; the tile-high ones again everywhere else)
 template <int MODE>
-sift_status dispatch(int tile, int hd, const CUtensorMap &mq, const CUtensorMap &mk,
-                     const CUtensorMap &mv, const AttnParams &p, cudaStream_t stream) {
-    if (tile == 128 && hd == 128) return launch_attention<128, 128, MODE>(mq, mk, mv, p, stream);
-    if (tile == 128 && hd == 64) return launch_attention<128, 64, MODE>(mq, mk, mv, p, stream);
-    if (tile == 64 && hd == 128) return launch_attention<64, 128, MODE>(mq, mk, mv, p, stream);
-    if (tile == 64 && hd == 64) return launch_attention<64, 64, MODE>(mq, mk, mv, p, stream);
+sift_status dispatch(int tile, int hd, const CUtensorMap *m, const AttnParams &p,
+                     cudaStream_t stream) {
+    if (tile == 128 && hd == 128)
+        return launch_attention<128, 128, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+    if (tile == 128 && hd == 64)
+        return launch_attention<128, 64, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+    if (tile == 64 && hd == 128)
+        return launch_attention<64, 128, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+    if (tile == 64 && hd == 64)
+        return launch_attention<64, 64, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
     return SIFT_ERR_UNSUPPORTED;
 }
 
@@ -968,6 +1072,8 @@ sift_status prepare(const sift_problem *prob, const void *q, const void *k, cons
         !make_map(&maps[1], k, d, prob->num_kv_heads, T, B) ||
         !make_map(&maps[2], v, d, prob->num_kv_heads, T, B))
         return SIFT_ERR_CUDA;
+    maps[3] = maps[1];
+    maps[4] = maps[2];
     const int N = num_query_tiles > 0 ? num_query_tiles : T / B;
     const int G = prob->num_q_heads / prob->num_kv_heads;
     AttnParams a{};
@@ -1007,7 +1113,7 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
     if (prob == nullptr || layer < 0 || layer >= prob->num_layers || kv_idx == nullptr ||
         counts == nullptr || sched == nullptr)
         return SIFT_ERR_INVALID_ARG;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
@@ -1017,14 +1123,15 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
     p.counts = counts + lu;
     p.sched = sched + lu;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<kModeList>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeList>(prob->tile, prob->head_dim, maps, p, stream);
 }
 
 extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int32_t num_query_tiles,
                                                   int32_t layer, const void *q, const void *k,
                                                   const void *v, const int32_t *qtiles,
                                                   const int32_t *kv, const int32_t *counts,
-                                                  const int32_t *sched, float softmax_scale,
+                                                  const int32_t *sched, const int32_t *pages,
+                                                  int32_t page_cap, float softmax_scale,
                                                   void *o, float *lse, void *workspace,
                                                   size_t workspace_bytes, int32_t *dev_status,
                                                   cudaStream_t stream) {
@@ -1033,9 +1140,13 @@ extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int3
         kv == nullptr || counts == nullptr || sched == nullptr || num_query_tiles < 1 ||
         (reinterpret_cast<uintptr_t>(kv) & 7u) != 0)
         return SIFT_ERR_INVALID_ARG;
+    const bool gather = gathers_pages(prob) && prob->num_docs > 0;
+    if (gather && (pages == nullptr || page_cap < 1 ||
+                   static_cast<int64_t>(prob->num_kv_heads) * prob->num_docs * page_cap > INT32_MAX))
+        return SIFT_ERR_INVALID_ARG;
     if (validate_ragged(prob, true) == SIFT_OK && num_query_tiles > max_query_tiles(prob))
         return SIFT_ERR_INVALID_ARG;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p, num_query_tiles);
@@ -1047,6 +1158,20 @@ extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int3
     p.qt = qtiles;
     p.B = prob->tile;
     const int page = prob->page ? prob->page : prob->tile;
+    p.page = page;
+    if (gather) {
+        const int64_t slice = static_cast<int64_t>(prob->num_kv_heads) * prob->num_docs * page_cap;
+        p.pages = pages + layer * slice;
+        p.pages_len = slice;
+        // gathered pages land page rows at a time (slot offsets are multiples of 1024 bytes,
+        // so the 128-byte swizzle phase of the tile is kept)
+        if (!make_map(&maps[3], k, prob->head_dim, prob->num_kv_heads, prob->total_tokens, page) ||
+            !make_map(&maps[4], v, prob->head_dim, prob->num_kv_heads, prob->total_tokens, page))
+            return SIFT_ERR_CUDA;
+    } else {
+        p.pages = nullptr;
+        p.pages_len = 0;
+    }
     const int pin = page < prob->tile ? page : prob->tile;
     int lp = 0;
     while ((1 << lp) < pin) ++lp;
@@ -1054,7 +1179,7 @@ extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int3
     p.full_info = static_cast<uint32_t>(prob->tile) |
                   ((1u << (prob->tile / pin)) - 1u) << 16;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<kModeRagged>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeRagged>(prob->tile, prob->head_dim, maps, p, stream);
 }
 
 extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const void *k,
@@ -1062,7 +1187,7 @@ extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
@@ -1078,7 +1203,7 @@ extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *
     p.counts = ws_counts;
     p.sched = ws_sched;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<kModeDense>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeDense>(prob->tile, prob->head_dim, maps, p, stream);
 }
 
 extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t layer,
@@ -1093,7 +1218,7 @@ extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t laye
         (prob->ca_words_len > 0 && ca_words == nullptr))
         return SIFT_ERR_INVALID_ARG;
     if (prob->num_prompts > kMaxFusedPrompts) return SIFT_ERR_UNSUPPORTED;
-    CUtensorMap maps[3];
+    CUtensorMap maps[5];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
@@ -1116,5 +1241,5 @@ extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t laye
     p.layer = layer;
     p.Hkv = prob->num_kv_heads;
     if (cudaMemsetAsync(workspace, 0, sizeof(int32_t), stream) != cudaSuccess) return SIFT_ERR_CUDA;
-    return dispatch<kModeBits>(prob->tile, prob->head_dim, maps[0], maps[1], maps[2], p, stream);
+    return dispatch<kModeBits>(prob->tile, prob->head_dim, maps, p, stream);
 }

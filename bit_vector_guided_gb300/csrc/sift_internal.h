@@ -27,6 +27,13 @@ sift_status validate_ragged(const sift_problem *p, bool attention);
 // upper bound on the per-segment query tiles: ceil(tokens/tile) + documents + prompts
 int64_t max_query_tiles(const sift_problem *p);
 
+// general layout: CA pages below the tile (and a multiple of 8 tokens) are gathered
+// into dense tiles rather than masked inside contiguous ones
+inline bool gathers_pages(const sift_problem *p) {
+    const int page = p->page ? p->page : p->tile;
+    return page < p->tile && page % 8 == 0;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // number of SMs of the current device (cached per device)

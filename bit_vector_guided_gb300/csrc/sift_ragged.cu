@@ -7,12 +7,15 @@
 //   ragged_tiles_kernel   one block: cuts every segment into query tiles (a block-wide
 //                         scan of the per-segment tile counts) and writes (first, rows);
 //   ragged_decode_kernel  one warp per (layer, kv head, segment): the CA prefix (tiles of
-//                         the earlier documents holding a flagged page) is compacted once
+//                         the earlier documents holding a flagged page, or -- for pages
+//                         below the tile -- the flagged whole pages gathered tile/page at
+//                         a time, then the flagged partial last pages) is compacted once
 //                         with ballots into the segment's first row and copied to the
 //                         others; each row then appends its LA tiles and its own tile;
 //   schedule_kernel       the longest-first order shared with the aligned decode.
-// List entries are (first token, info) pairs, info = len | causal << 8 | mask << 16
-// (the format and its reading are stated in include/sift.h).
+// List entries are (first token, info) pairs, info = len | causal << 8 | gather << 9 |
+// mask << 16; a gathered entry's first field indexes the page array instead (the format
+// and its reading are stated in include/sift.h).
 #include "sift_internal.h"
 
 namespace sift {
@@ -27,8 +30,10 @@ struct RaggedArgs {
     const uint64_t *la, *ca;
     int64_t la_len, ca_len;
     int32_t *qt, *kv, *counts, *status;
-    int P, D, Hkv, L, B, page, NQ, rowcap;
-    uint32_t full;  // mask bits of a tile with every page kept
+    int32_t *pages;  // gathered pages [L][Hkv][D][page_cap] (gather only)
+    int P, D, Hkv, L, B, page, NQ, rowcap, page_cap;
+    uint32_t full;   // mask bits of a tile with every page kept
+    bool gather;     // page < tile and a multiple of 8: CA pages are gathered into tiles
 };
 
 __device__ __forceinline__ void rstatus(int32_t *st, int code) { atomicCAS(st, 0, code); }
@@ -172,7 +177,80 @@ __global__ void __launch_bounds__(kRaggedWarps * 32) ragged_decode_kernel(Ragged
     // ---- prefix: tiles of the earlier documents, into the first row's list
     const int64_t r0 = row_of(qfirst);
     int npre = 0;
-    for (int gp = sg.g0; gp < g_end; ++gp) {
+    if (!suffix && a.gather) {
+        // whole flagged pages of the earlier documents, ascending, into the page array
+        const int64_t pbase = (static_cast<int64_t>(lh) * a.D + sg.g) * a.page_cap;
+        const int64_t rel = (static_cast<int64_t>(h) * a.D + sg.g) * a.page_cap;
+        int npg = 0;
+        for (int gp = sg.g0; gp < g_end; ++gp) {
+            const int ds = (gp == sg.g0) ? __ldg(a.cu + sg.p) : __ldg(a.doc_end + gp - 1);
+            const int de = __ldg(a.doc_end + gp);
+            if (de < ds) {
+                if (lane == 0) rstatus(a.status, SIFT_ERR_DEVICE_CHECK);
+                continue;
+            }
+            const int C = (de - ds + a.page - 1) / a.page;
+            const int V = (C + 63) / 64;
+            const int64_t off = __ldg(a.ca_off + gp) + static_cast<int64_t>(lh) * V;
+            if (off < 0 || off + V > a.ca_len) {
+                if (lane == 0) rstatus(a.status, SIFT_ERR_DEVICE_CHECK);
+                continue;
+            }
+            const int whole = (de - ds) / a.page;
+            for (int j0 = 0; j0 < whole; j0 += 32) {
+                const int j = j0 + static_cast<int>(lane);
+                const bool inc = j < whole && ((__ldg(a.ca + off + j / 64) >> (j % 64)) & 1ull);
+                const uint32_t bal = __ballot_sync(kAll, inc);
+                const int pos = npg + __popc(bal & lt);
+                if (inc && pos < a.page_cap) a.pages[pbase + pos] = ds + j * a.page;
+                npg += __popc(bal);
+            }
+        }
+        if (npg > a.page_cap) {
+            if (lane == 0) rstatus(a.status, SIFT_ERR_DEVICE_CHECK);
+            npg = a.page_cap;
+        }
+        const int per = a.B / a.page;
+        const int ngroups = (npg + per - 1) / per;
+        for (int k = static_cast<int>(lane); k < ngroups; k += 32) {
+            const int pos = npre + k;
+            if (pos < a.rowcap) {
+                const int in_group = min(per, npg - k * per);
+                a.kv[2 * (r0 + pos)] = static_cast<int32_t>(rel + k * per);
+                a.kv[2 * (r0 + pos) + 1] = static_cast<int32_t>(
+                    static_cast<uint32_t>(in_group * a.page) | 1u << 9 | a.full << 16);
+            }
+        }
+        npre += ngroups;
+        // then each earlier document's last page when it is partial and flagged
+        for (int gb = sg.g0; gb < g_end; gb += 32) {
+            const int gp = gb + static_cast<int>(lane);
+            bool inc = false;
+            int first = 0, rem = 0;
+            if (gp < g_end) {
+                const int ds = (gp == sg.g0) ? __ldg(a.cu + sg.p) : __ldg(a.doc_end + gp - 1);
+                const int de = __ldg(a.doc_end + gp);
+                rem = de >= ds ? (de - ds) % a.page : 0;
+                if (rem) {
+                    const int C = (de - ds + a.page - 1) / a.page;
+                    const int V = (C + 63) / 64;
+                    const int64_t off = __ldg(a.ca_off + gp) + static_cast<int64_t>(lh) * V;
+                    const int j = C - 1;
+                    inc = off >= 0 && off + V <= a.ca_len &&
+                          ((__ldg(a.ca + off + j / 64) >> (j % 64)) & 1ull);
+                    first = de - rem;
+                }
+            }
+            const uint32_t bal = __ballot_sync(kAll, inc);
+            const int pos = npre + __popc(bal & lt);
+            if (inc && pos < a.rowcap) {
+                a.kv[2 * (r0 + pos)] = first;
+                a.kv[2 * (r0 + pos) + 1] = static_cast<int32_t>(static_cast<uint32_t>(rem) | 1u << 16);
+            }
+            npre += __popc(bal);
+        }
+    }
+    for (int gp = sg.g0; gp < g_end && !(!suffix && a.gather); ++gp) {
         const int ds = (gp == sg.g0) ? __ldg(a.cu + sg.p) : __ldg(a.doc_end + gp - 1);
         const int de = __ldg(a.doc_end + gp);
         if (de < ds) {
@@ -274,8 +352,8 @@ __global__ void __launch_bounds__(kRaggedWarps * 32) ragged_decode_kernel(Ragged
 extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles,
                                           const uint64_t *la_words, const uint64_t *ca_words,
                                           int32_t *qtiles, int32_t *kv, int32_t *counts,
-                                          int32_t *sched, int32_t *dev_status,
-                                          cudaStream_t stream) {
+                                          int32_t *sched, int32_t *pages, int32_t page_cap,
+                                          int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
     sift_status st = validate_ragged(prob, false);
     if (st != SIFT_OK) return st;
@@ -286,7 +364,15 @@ extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_
     if ((prob->la_words_len > 0 && la_words == nullptr) ||
         (prob->ca_words_len > 0 && ca_words == nullptr))
         return SIFT_ERR_INVALID_ARG;
+    const bool gather = gathers_pages(prob);
+    if (gather && prob->num_docs > 0 &&
+        (pages == nullptr || page_cap < 1 ||
+         static_cast<int64_t>(prob->num_kv_heads) * prob->num_docs * page_cap > INT32_MAX))
+        return SIFT_ERR_INVALID_ARG;
     RaggedArgs a{};
+    a.pages = pages;
+    a.page_cap = gather ? page_cap : 0;
+    a.gather = gather;
     a.cu = prob->cu_seqlens;
     a.doc_cu = prob->doc_cu;
     a.doc_end = prob->doc_end;

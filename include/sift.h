@@ -94,7 +94,8 @@ typedef struct {
     int32_t total_tokens;          /* cu_seqlens[P]                                     */
     int32_t max_tiles_per_prompt;  /* rowcap: capacity of one list row, >= the key tiles of
                                       the longest prompt (ragged: the sum over its segments
-                                      of ceil(length/tile))                             */
+                                      of ceil(length/tile), plus its number of documents
+                                      when CA pages are gathered)                       */
     int32_t page;                  /* CA page size in tokens; 0 = tile.  The aligned entry
                                       points need 0 or tile; the ragged ones a power of two
                                       that nests with tile, at most 16 pages per tile   */
@@ -271,7 +272,8 @@ sift_status sift_build_bits(const sift_problem *prob, int32_t layer, const void 
  *           LA-flagged tiles below the row inside its own document, then the
  *           row's own tile; a suffix row lists every tile of its prompt's
  *           documents, its earlier suffix tiles, then its own tile.
- *           info = len | causal << 8 | mask << 16, Pin = min(page, tile):
+ *           info = len | causal << 8 | gather << 9 | mask << 16, with
+ *           Pin = min(page, tile):
  *             len    keys of the tile inside its segment (1 .. tile);
  *             causal 1 on the row's own tile only;
  *             mask   bit k covers keys [k*Pin, (k+1)*Pin) of the tile: the
@@ -279,15 +281,27 @@ sift_status sift_build_bits(const sift_problem *prob, int32_t layer, const void 
  *           Key (first + c) is visible to query row r iff c < len, mask bit
  *           c/Pin is set and, when causal, c <= r.  Entries past the count
  *           are not written.
+ *           Gathered pages (page < tile and page a multiple of 8): a document
+ *           row's CA part lists instead the whole flagged pages of the
+ *           earlier documents, tile/page at a time (gather = 1, len = pages x
+ *           page, first = index of the group's first page in the layer's
+ *           slice of `pages`; key c is token pages[first + c/page] + c%page),
+ *           then each earlier document's partial last page when flagged.
  *   counts  int32 [num_layers][Hkv][num_query_tiles]
  *   sched   int32 [num_layers][Hkv*num_query_tiles]: per layer, a permutation
  *           of the units u = h*num_query_tiles + q with non-increasing counts.
- * Bit-exact for qtiles, kv and counts.  Three kernel launches.
+ *   pages   int32 [num_layers][Hkv][num_docs][page_cap]: for the rows of
+ *           document g, the first tokens of the gathered pages, ascending.
+ *           Needed (non-NULL, page_cap >= the flagged whole pages before any
+ *           document; tile/page x max_tiles_per_prompt always suffices) only
+ *           when pages are gathered; NULL and 0 otherwise.
+ * Bit-exact for qtiles, kv, counts and the pages used.  Three kernel launches.
  */
 sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles,
                                const uint64_t *la_words, const uint64_t *ca_words,
                                int32_t *qtiles, int32_t *kv, int32_t *counts, int32_t *sched,
-                               int32_t *dev_status, cudaStream_t stream);
+                               int32_t *pages, int32_t page_cap, int32_t *dev_status,
+                               cudaStream_t stream);
 
 /*
  * Block-sparse causal grouped-query flash attention of one layer on a general
@@ -295,13 +309,16 @@ sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles
  * attends to the visible keys of the entries of row
  * (layer, qh / (Hq/Hkv), q).  Same q, k, v, o, lse layouts and workspace as
  * sift_sparse_prefill (total_tokens need not be a multiple of tile); only the
- * rows of each query tile inside its segment are written.
+ * rows of each query tile inside its segment are written.  Gathered pages
+ * are loaded by TMA page rows at a time side by side into one key tile.
+ * qtiles, kv, counts, sched, pages, page_cap: as from sift_decode_ragged.
  * One memset and one kernel launch.
  */
 sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int32_t num_query_tiles,
                                        int32_t layer, const void *q, const void *k,
                                        const void *v, const int32_t *qtiles, const int32_t *kv,
                                        const int32_t *counts, const int32_t *sched,
+                                       const int32_t *pages, int32_t page_cap,
                                        float softmax_scale, void *o, float *lse,
                                        void *workspace, size_t workspace_bytes,
                                        int32_t *dev_status, cudaStream_t stream);

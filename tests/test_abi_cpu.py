@@ -91,11 +91,11 @@ def test_host_validation_pointers_and_sizes(lib):
 def test_ragged_host_validation(lib, over, nq, code):
     p = _struct(**over)
     d = ctypes.c_void_p(256)
-    rc = lib.sift_sparse_prefill_ragged(ctypes.byref(p), nq, 0, d, d, d, d, d, d, d, 0.0, d, d,
-                                        d, 1 << 20, d, None)
+    rc = lib.sift_sparse_prefill_ragged(ctypes.byref(p), nq, 0, d, d, d, d, d, d, d, d, 1, 0.0,
+                                        d, d, d, 1 << 20, d, None)
     assert rc == code
     if code == 2 and "head_dim" not in over and "num_q_heads" not in over:
-        assert lib.sift_decode_ragged(ctypes.byref(p), max(nq, 1), d, d, d, d, d, d, d,
+        assert lib.sift_decode_ragged(ctypes.byref(p), max(nq, 1), d, d, d, d, d, d, d, 1, d,
                                       None) == 2
 
 
@@ -111,4 +111,10 @@ def test_ragged_layout_rules(lib):
     # misaligned list pointer (entries are 8-byte pairs)
     p = _struct(total_tokens=200)
     assert lib.sift_sparse_prefill_ragged(ctypes.byref(p), 2, 0, d, d, d, d, ctypes.c_void_p(260),
-                                          d, d, 0.0, d, d, d, 1 << 20, d, None) == 1
+                                          d, d, d, 1, 0.0, d, d, d, 1 << 20, d, None) == 1
+    # gathered pages (page 16 < tile 128) without a page array
+    p = _struct(total_tokens=200, page=16, num_docs=1, doc_end=ctypes.c_void_p(64),
+                la_off=ctypes.c_void_p(64), ca_off=ctypes.c_void_p(64))
+    assert lib.sift_sparse_prefill_ragged(ctypes.byref(p), 2, 0, d, d, d, d, d, d, d, None, 0,
+                                          0.0, d, d, d, 1 << 20, d, None) == 1
+    assert lib.sift_decode_ragged(ctypes.byref(p), 2, d, d, d, d, d, d, None, 0, d, None) == 1

@@ -45,10 +45,10 @@ def _setup(sift, cfg):
 
 def _check_decode(sift, lay, la, ca, prob, la_d, ca_d):
     st = prob.new_status()
-    qt, kv, cnt, sched = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
+    qt, kv, cnt, sched, pages = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0, sift.status_string(int(st.item()))
-    qt_o, kv_o, cnt_o = oracle.decode_ragged(lay, la, ca)
+    qt_o, kv_o, cnt_o, pg_o = oracle.decode_ragged(lay, la, ca, page_cap=prob.page_cap)
     assert np.array_equal(qt.cpu().numpy(), qt_o)
     cnt_h = cnt.cpu().numpy()
     assert np.array_equal(cnt_h, cnt_o)
@@ -60,7 +60,18 @@ def _check_decode(sift, lay, la, ca, prob, la_d, ca_d):
                 n = cnt_h[l, h, q]
                 assert np.array_equal(kv_h[l, h, q, :n], kv_o[l, h, q, :n]), (l, h, q)
     check_sched(sched.cpu().numpy(), cnt_h)
-    return qt, kv, cnt, sched
+    if pages is not None:  # gathered pages: every page a list points at, bit-exact
+        pg_h = pages.cpu().numpy()
+        for l in range(L):
+            for h in range(H):
+                for q in range(NQ):
+                    for first, info in kv_h[l, h, q, :cnt_h[l, h, q]]:
+                        if (int(info) >> 9) & 1:
+                            n = (int(info) & 0xFF) // lay.page_size
+                            got = pg_h[l].reshape(-1)[first: first + n]
+                            want = pg_o[l].reshape(-1)[first: first + n]
+                            assert np.array_equal(got, want), (l, h, q, first)
+    return qt, kv, cnt, sched, pages
 
 
 CFGS = [
@@ -82,6 +93,15 @@ CFGS = [
                     num_q_heads=2, num_kv_heads=1, head_dim=128, tile=64),
     W.custom_config("rg_e", [([100, 150, 31], 17)], W.BitSpec(la_p=0.3, ca_p=0.2),
                     num_q_heads=2, num_kv_heads=1, head_dim=128, tile=64, page=4),
+    # gathered pages: 16 pages of 8 tokens per tile; 2 pages of 64
+    W.custom_config("rg_f", [([333, 250, 129, 64], 40)], W.BitSpec(la_p=0.3, ca_p=0.25),
+                    num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128, page=8),
+    W.custom_config("rg_g", [([333, 250, 129, 64], 40)], W.BitSpec(la_p=0.3, ca_p=0.4),
+                    num_q_heads=4, num_kv_heads=2, head_dim=64, tile=128, page=64),
+    # many tiny documents: more gathered partial pages than whole tiles
+    W.custom_config("rg_tiny", [([17] * 20, 0), ([1, 2, 3, 17, 33], 5)],
+                    W.BitSpec(pattern="ones"), num_q_heads=2, num_kv_heads=1, head_dim=128,
+                    tile=128, page=16),
     # every bit set / none
     W.custom_config("rg_ones", [([300, 99, 77], 50), ([1000], 5)], W.BitSpec(pattern="ones"),
                     num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128, page=16),
@@ -93,11 +113,11 @@ CFGS = [
 @pytest.mark.parametrize("cfg", CFGS, ids=lambda c: c.name)
 def test_ragged_decode_and_attention_match_oracle(sift, cfg):
     lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
-    qt, kv, cnt, sched = _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
+    qt, kv, cnt, sched, pages = _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
     st = prob.new_status()
     for layer in range(cfg.num_layers):
         q, k, v = W.make_qkv(cfg, layer, device="cuda")
-        o, lse = sift.sparse_prefill_ragged(prob, layer, q, k, v, qt, kv, cnt, sched,
+        o, lse = sift.sparse_prefill_ragged(prob, layer, q, k, v, qt, kv, cnt, sched, pages,
                                             dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0, sift.status_string(int(st.item()))
@@ -111,11 +131,11 @@ def test_ragged_rows_outside_segments_are_not_written(sift):
     the partial tiles' missing rows are the next segment's, not garbage."""
     cfg = CFGS[0]
     lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
-    qt, kv, cnt, sched = sift.decode_ragged(prob, la_d, ca_d)
+    qt, kv, cnt, sched, pages = sift.decode_ragged(prob, la_d, ca_d)
     q, k, v = W.make_qkv(cfg, 0, device="cuda")
     o = torch.full_like(q, float("nan"))
     lse = torch.full((cfg.num_q_heads, lay.total_tokens), float("nan"), device="cuda")
-    sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv, cnt, sched, o=o, lse=lse)
+    sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv, cnt, sched, pages, o=o, lse=lse)
     torch.cuda.synchronize()
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 
@@ -130,7 +150,7 @@ def test_general_path_equals_aligned_path_on_aligned_layout(sift, name):
     assert lay.aligned
     st = prob.new_status()
     kv_a, cnt_a, sch_a = sift.decode(prob, la_d, ca_d, dev_status=st)
-    qt, kv_r, cnt_r, sch_r = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
+    qt, kv_r, cnt_r, sch_r, _ = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
     q, k, v = W.make_qkv(cfg, 0, device="cuda")
     o1, l1 = sift.sparse_prefill(prob, 0, q, k, v, kv_a, cnt_a, sch_a, dev_status=st)
     o2, l2 = sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv_r, cnt_r, sch_r, dev_status=st)
@@ -148,7 +168,7 @@ def test_ragged_full_size_workload(sift):
     import dataclasses
     cfg = dataclasses.replace(full, num_layers=2)
     lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
-    qt, kv, cnt, sched = _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
+    qt, kv, cnt, sched, pages = _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
     qt_h = qt.cpu().numpy()
     rng = np.random.default_rng(7)
     partial = [i for i, (_, r) in enumerate(qt_h) if r < lay.tile]
@@ -157,7 +177,7 @@ def test_ragged_full_size_workload(sift):
     st = prob.new_status()
     for layer in range(cfg.num_layers):
         q, k, v = W.make_qkv(cfg, layer, device="cuda")
-        o, lse = sift.sparse_prefill_ragged(prob, layer, q, k, v, qt, kv, cnt, sched,
+        o, lse = sift.sparse_prefill_ragged(prob, layer, q, k, v, qt, kv, cnt, sched, pages,
                                             dev_status=st)
         torch.cuda.synchronize()
         assert int(st.item()) == 0

@@ -130,6 +130,10 @@ RAGGED_CFGS = [
     W.custom_config("rg_p64", [([200, 130, 64], 0), ([77], 5)],
                     W.BitSpec(head_density=(0.1, 0.7)), num_layers=2, num_q_heads=4,
                     num_kv_heads=2, head_dim=4, tile=16, page=64),
+    # many tiny documents with gathered pages: more partial pages than whole tiles
+    W.custom_config("rg_tiny", [([17] * 20, 0), ([1, 2, 3, 17, 33], 5)],
+                    W.BitSpec(la_p=0.5, ca_p=0.7), num_q_heads=2, num_kv_heads=1, head_dim=4,
+                    tile=128, page=16),
     # 65 pages (8 * 64 + 3 tokens): the CA block of each (layer, head) takes two words
     W.custom_config("rg_cross", [([8 * 64 + 3, 20], 4)], W.BitSpec(la_p=0.2, ca_p=0.5),
                     num_layers=2, num_q_heads=4, num_kv_heads=2, head_dim=4, tile=16, page=8),

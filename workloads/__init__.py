@@ -249,6 +249,9 @@ def make_layout(cfg: Config) -> Layout:
         pos += suf
         cu.append(pos)
         doc_cu.append(len(doc_end))
+        if Pg < B and Pg % 8 == 0:
+            # gathered CA pages: each earlier document may add its partial last page
+            tiles += len(docs)
         max_tiles = max(max_tiles, tiles)
     return Layout(
         num_prompts=len(cfg.prompts), num_docs=len(doc_end), num_layers=cfg.num_layers,
