@@ -42,6 +42,7 @@ import workloads as W  # noqa: E402
 METRIC = "sparse-prefill attention TFLOP/s (computed tiles) & % bf16 peak; ms per layer vs dense"
 UNIT = "TFLOP/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sift_sparse_prefill_llama_32k.md")
+PROFILE_RAGGED = os.path.join(ROOT, "profiles", "sift_sparse_prefill_ragged_llama_32k_ragged.md")
 
 
 def tile_flops(cfg) -> float:
@@ -74,13 +75,13 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the sparse kernel from the committed ncu summary, if it was
+def profiled_traffic(path=PROFILE_SUMMARY):
+    """DRAM bytes per launch of the sparse kernel from a committed ncu summary, if it was
     taken on the current kernel source (else None)."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    if not os.path.exists(path):
         return None
     vals = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and line.strip().startswith("- "):
                 k, _, v = line.strip()[2:].partition(":")
@@ -609,13 +610,14 @@ def run_sweep(args, dev, stream):
     return rows
 
 
-def run_ragged(args, dev, stream):
-    """The general-layout step on the ragged 33K workload: sift_decode_ragged of all layers,
-    then one sift_sparse_prefill_ragged per layer; dense causal attention over the same
-    prompts (documents play no part in it) is timed beside it."""
+def run_ragged(args, dev, stream, cfg=None, steps=3, warmup=2):
+    """The general-layout step on a ragged workload (default: the ragged 33K one):
+    sift_decode_ragged of all layers, then one sift_sparse_prefill_ragged per layer; dense
+    causal attention over the same prompts (documents play no part in it) is timed beside
+    it."""
     import torch
     import bit_vector_guided_gb300 as sift
-    cfg = W.get_config("llama_32k_ragged")
+    cfg = cfg or W.get_config("llama_32k_ragged")
     L = cfg.num_layers
     lay = W.make_layout(cfg)
     la, ca = W.make_bits(cfg, lay)
@@ -650,10 +652,9 @@ def run_ragged(args, dev, stream):
             if record:
                 ev[2 + l].record(stream)
 
-    for _ in range(2):
+    for _ in range(max(warmup, 1)):
         step()
     torch.cuda.synchronize(dev)
-    steps = 3
     layer_ms, dec_ms, step_ms = [], [], []
     for _ in range(steps):
         step(record=True)
@@ -685,7 +686,8 @@ def run_ragged(args, dev, stream):
     peaks, _ = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     ktf = float(fl.mean()) / (kern_ms * 1e-3) / 1e12
-    return {"workload": cfg.name, "page": cfg.page, "query_tiles": NQ,
+    return {"workload": cfg.name, "page": cfg.page, "query_tiles": NQ, "layers": L,
+            "flops_per_step": float(fl.sum()),
             "ms_per_step": float(np.mean(step_ms)),
             "tflops": float(fl.sum()) / (float(np.mean(step_ms)) * 1e-3) / 1e12,
             "sparse_ms_per_layer": kern_ms, "kernel_tflops": ktf,
@@ -725,7 +727,43 @@ def main(argv=None):
                                   f" [first {args.layers} layers only]")
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if not W.make_layout(cfg).aligned:
+        return run_ragged_line(args, cfg)
     return run_ours(args, cfg)
+
+
+def run_ragged_line(args, cfg):
+    """A workload of the general layout as the measured step (one GPU): one JSON line."""
+    import torch
+    import bit_vector_guided_gb300 as sift
+    from bit_vector_guided_gb300 import build as sbuild
+    if args.gpus > 1:
+        raise SystemExit("the general-layout workloads run on one GPU")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sbuild.build()
+    sift.load_library()
+    stream = torch.cuda.current_stream(dev)
+    with ClockSampler(0) as clk:
+        r = run_ragged(args, dev, stream, cfg=cfg, steps=args.steps, warmup=args.warmup)
+    lay = W.make_layout(cfg)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    out = {
+        "metric": METRIC, "value": r["tflops"], "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(cfg, args, lay),
+        "roofline": {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
+                     "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak,
+                     "traffic": profiled_traffic(PROFILE_RAGGED),
+                     "kernel": "sift_sparse_prefill_ragged",
+                     "peak_source": f"bf16_tflops_sustained of {peak_src}"},
+        "gpu_launches": args.steps * r["gpu_launches_per_step"], "ragged": r,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(out))
+    return 0
 
 
 if __name__ == "__main__":
