@@ -51,9 +51,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     nvcc = nvcc_path()
     objs = []
+    # objects of this process only: concurrent builds (parallel test workers) never share
+    # a half-written file; the library itself is replaced atomically
+    obj_dir = os.path.join(OUT_DIR, f"obj.{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -70,6 +74,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB
 
 
