@@ -48,3 +48,35 @@ def test_stalled_wait_times_out_cleanly(sift):
     O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
     assert_attention_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), O, LSE,
                            "after timeout")
+
+
+def test_stalled_wait_times_out_cleanly_general_layout(sift):
+    """The same on the general layout with gathered pages in flight: the producers' page
+    copies are drained like whole-tile ones before the kernel returns."""
+    cfg = W.custom_config("watchdog_rg", [([300, 411, 77], 50)], W.BitSpec(la_p=0.3, ca_p=0.4),
+                          num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128, page=16)
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, "cuda")
+    from helpers import device_bits
+    la_d, ca_d = device_bits(la, ca)
+    st = prob.new_status()
+    lists = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    sift.debug_set_waits(timeout_ns=2_000_000, stall=True)
+    try:
+        st = prob.new_status()
+        sift.sparse_prefill_ragged(prob, 0, q, k, v, *lists, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 4, sift.status_string(int(st.item()))  # SIFT_ERR_TIMEOUT
+    finally:
+        sift.debug_set_waits(0, False)
+    st = prob.new_status()
+    o, lse = sift.sparse_prefill_ragged(prob, 0, q, k, v, *lists, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    assert_attention_close(o.double().cpu().numpy(), lse.double().cpu().numpy(), O, LSE,
+                           "general layout after timeout")
