@@ -56,6 +56,23 @@ def computed_flops(cfg, counts: np.ndarray) -> np.ndarray:
     return counts.reshape(counts.shape[0], -1).sum(axis=1).astype(np.float64) * G * tile_flops(cfg)
 
 
+def decode_bytes(lay, counts: np.ndarray) -> float:
+    """Algorithmic bytes of one decode of all layers: LA/CA words read, kv entries, counts
+    and schedule written, counts read again by the schedule."""
+    units = counts.size
+    return float(8 * (lay.la_words_len + lay.ca_words_len) + 4 * int(counts.sum()) +
+                 4 * units + 4 * units + 4 * units)
+
+
+def useful_fraction(cfg, lay, flops_step: float) -> float:
+    """Share of the computed-tile FLOPs that are not masked out on the diagonal: every row
+    holds one diagonal tile, of which (B+1)/(2B) is causal."""
+    B = cfg.tile
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    diag = cfg.num_layers * cfg.num_kv_heads * lay.num_tiles * G * tile_flops(cfg)
+    return (flops_step - diag * (B - 1) / (2 * B)) / flops_step
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -454,6 +471,12 @@ def run_ours(args, cfg):
         "speedup_vs_dense": dense_ms_layer / kern_ms,
         "computed_tile_fraction": float(flops_layer.mean() / dense_flops_layer),
         "decode_us": 1e3 * float(np.median(decode_ms)),
+        # decode's algorithmic bytes: every bit word read once; lists, counts and the
+        # schedule written once (counts read back by the schedule)
+        "decode_gbs": decode_bytes(lay, counts_h) / (float(np.median(decode_ms)) * 1e-3) / 1e9,
+        "decode_bytes": decode_bytes(lay, counts_h),
+        # diagonal tiles counted at the (B+1)/(2B) of their entries that are causal
+        "useful_tflops": value * useful_fraction(cfg, lay, flops_step),
         "fused_ms_per_step": fused_ms_step,
         "fused_ms_per_layer": fused_ms_step / L,
         "fused_tflops": flops_step / (fused_ms_step * 1e-3) / 1e12,

@@ -92,3 +92,44 @@ def gpu_rows(o_gpu, lse_gpu, tok, head):
     lse = lse_gpu[torch.as_tensor(head, device=o_gpu.device).long(),
                   torch.as_tensor(tok, device=o_gpu.device).long()].double().cpu().numpy()
     return o, lse
+
+
+def enumerated_prompts():
+    """Every LA/CA bit pattern of a prompt with two 3-tile documents and a 1-tile suffix:
+    6 meaningful LA bits (rows 1 and 2 of each document) and the 3 CA bits of the first
+    document (the second's CA has no later document), 2^9 = 512 patterns, each its own
+    prompt in one batch.  Returns (layout, la_words, ca_words, patterns)."""
+    B, T = 4, 3
+    n = 1 << 9
+    cfg = W.custom_config("enum", [([B * T, B * T], B)] * n, W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=4, tile=B)
+    lay = W.make_layout(cfg)
+    la = np.zeros(lay.la_words_len, np.uint64)
+    ca = np.zeros(lay.ca_words_len, np.uint64)
+    for pat in range(n):
+        g0, g1 = 2 * pat, 2 * pat + 1
+        bits = [(pat >> b) & 1 for b in range(9)]
+        # document 0: LA rows 1 (bit 0 -> j=0) and 2 (bits 1, 2 -> j=0, 1)
+        la[lay.la_off[g0] + 1] = np.uint64(bits[0])
+        la[lay.la_off[g0] + 2] = np.uint64(bits[1] | bits[2] << 1)
+        la[lay.la_off[g1] + 1] = np.uint64(bits[3])
+        la[lay.la_off[g1] + 2] = np.uint64(bits[4] | bits[5] << 1)
+        ca[lay.ca_off[g0]] = np.uint64(bits[6] | bits[7] << 1 | bits[8] << 2)
+    return lay, la, ca, n
+
+
+def plain_lists(pat, p0):
+    """The list rule for one enumerated prompt starting at global tile p0, written out:
+    document-0 rows: own LA tiles then the diagonal; document-1 rows: document 0's CA
+    pages, own LA tiles, the diagonal; the suffix row: every tile up to itself."""
+    bits = [(pat >> b) & 1 for b in range(9)]
+    la0 = {1: [0] if bits[0] else [], 2: [j for j, b in ((0, bits[1]), (1, bits[2])) if b]}
+    la1 = {1: [0] if bits[3] else [], 2: [j for j, b in ((0, bits[4]), (1, bits[5])) if b]}
+    ca0 = [j for j in range(3) if bits[6 + j]]
+    rows = []
+    for i in range(3):
+        rows.append([p0 + j for j in la0.get(i, [])] + [p0 + i])
+    for i in range(3):
+        rows.append([p0 + j for j in ca0] + [p0 + 3 + j for j in la1.get(i, [])] + [p0 + 3 + i])
+    rows.append(list(range(p0, p0 + 7)))
+    return rows

@@ -150,3 +150,23 @@ def test_decode_rejects_bad_arguments(sift):
     with pytest.raises(sift.SiftError) as e:
         sift.decode(prob, None, ca_d)
     assert e.value.code == 1
+
+
+def test_decode_exhaustive_tiny_patterns_bit_exact(sift):
+    """All 512 LA/CA patterns of a two-document, three-tile prompt, as one batch of 512
+    prompts: the GPU lists equal the oracle's and the list rule written out."""
+    from helpers import enumerated_prompts, plain_lists
+    lay, la, ca, n = enumerated_prompts()
+    prob = sift.SiftProblem.from_layout(lay, "cuda")
+    la_d, ca_d = device_bits(la, ca)
+    st = prob.new_status()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kv_h, cnt_h = kv.cpu().numpy(), cnt.cpu().numpy()
+    kv_o, cnt_o = oracle.decode(lay, la, ca)
+    assert np.array_equal(cnt_h, cnt_o)
+    for pat in range(n):
+        for r, want in enumerate(plain_lists(pat, 7 * pat)):
+            i = 7 * pat + r
+            assert list(kv_h[0, 0, i, :cnt_h[0, 0, i]]) == want, (pat, r)

@@ -374,3 +374,16 @@ def test_build_counts_follow_the_fractions():
         for i in range(T):
             assert bin(int(la[base + i])).count("1") == int(np.ceil(0.25 * i - 1e-4))
         assert bin(int(ca[lay.ca_off[g]])).count("1") == int(np.ceil(0.4 * T - 1e-4))
+
+
+# ---- exhaustive decode on tiny prompts ----------------------------------------------
+
+def test_decode_exhaustive_tiny_patterns():
+    """Every LA/CA pattern of a two-document prompt against the list rule written out."""
+    from helpers import enumerated_prompts, plain_lists
+    lay, la, ca, n = enumerated_prompts()
+    kv, cnt = oracle.decode(lay, la, ca)
+    for pat in range(n):
+        for r, want in enumerate(plain_lists(pat, 7 * pat)):
+            i = 7 * pat + r
+            assert list(kv[0, 0, i, :cnt[0, 0, i]]) == want, (pat, r)
