@@ -38,7 +38,7 @@ _lib = None
 __all__ = ["build", "load", "decode", "schedule", "attention_rows", "attention_all",
            "key_mask", "brute_force_attention", "tile_mask", "set_threads", "decode_ragged",
            "token_mask", "page_capacity",
-           "doc_tile_masses", "top_count", "select_top", "build_bits"]
+           "doc_tile_masses", "doc_unit_masses", "top_count", "select_top", "build_bits"]
 
 
 def build(force: bool = False) -> str:
@@ -386,34 +386,72 @@ def select_top(mass: np.ndarray, kcount: int) -> np.ndarray:
     return np.array(sorted(order[:kcount]), dtype=np.int64)
 
 
+def doc_unit_masses(q, k, start, end, h, G, tile, unit, scale):
+    """Mu[i][u]: attention probability mass that the query rows of tile i (all query heads of
+    kv head h's group; tiles of `tile` tokens from the document start, the last partial) put
+    on key unit u (units of `unit` tokens, counted the same way), in causal attention inside
+    the document [start, end) alone.  Row i sums to G x (rows of tile i)."""
+    qf = np.asarray(_bf16_bits(q[start:end, h * G:(h + 1) * G]).astype(np.uint32) << 16
+                    ).view(np.float32).astype(np.float64)
+    kf = np.asarray(_bf16_bits(k[start:end, h:h + 1]).astype(np.uint32) << 16
+                    ).view(np.float32).astype(np.float64)[:, 0]
+    n = end - start
+    causal = np.tril(np.ones((n, n), bool))
+    P = np.zeros((n, n))
+    for g in range(G):
+        S = scale * qf[:, g, :] @ kf.T
+        S = np.where(causal, S, -np.inf)
+        S -= S.max(axis=1, keepdims=True)
+        Pm = np.exp(S)
+        P += Pm / Pm.sum(axis=1, keepdims=True)
+    rows = np.add.reduceat(P, np.arange(0, n, tile), axis=0)
+    return np.add.reduceat(rows, np.arange(0, n, unit), axis=1)
+
+
 def build_bits(layout, layer, q, k, la_fraction, ca_fraction, scale=None):
-    """LA/CA words of one layer from document-alone attention (the offline profiler):
+    """LA/CA words of one layer from document-alone attention (the offline profiler).
+    Tiles and pages are counted from each document's first token (the last ones partial);
+    masses are gathered per unit of min(page, tile) tokens:
+      M[i][j]  = mass that query tile i puts on key tile j (its units summed);
       LA row i keeps the top_count(la_fraction, i) tiles j < i of largest M[i][j];
-      CA keeps the top_count(ca_fraction, T) pages j of largest mean mass received from
-      the document's rows i >= j, sum_{i>=j} M[i][j] / (T - j).
-    Returns (la_words, ca_words, masses) with the layer's blocks filled (other layers 0)
-    and masses[(g, h)] = M for validation."""
+      page c, whose first token lies in tile t(c), scores the mean mass it receives from
+      the query tiles i >= t(c), sum_{i >= t(c)} mass_i(c) / (T - t(c));
+      CA keeps the top_count(ca_fraction, C) pages of largest score.
+    With page == tile this is the tile rule: score(j) = sum_{i>=j} M[i][j] / (T - j).
+    Returns (la_words, ca_words, masses, scores) with the layer's blocks filled (other
+    layers 0), masses[(g, h)] = M and scores[(g, h)] = the page scores, for validation."""
     B, Hkv = layout.tile, layout.num_kv_heads
+    Pg = _page(layout)
+    U = min(Pg, B)
     G = layout.num_q_heads // Hkv
     scale = (1.0 / np.sqrt(layout.head_dim)) if scale is None else float(scale)
     la = np.zeros(layout.la_words_len, np.uint64)
     ca = np.zeros(layout.ca_words_len, np.uint64)
-    masses = {}
+    masses, scores = {}, {}
     for g in range(layout.num_docs):
         s0, e0 = layout.doc_start(g), int(layout.doc_end[g])
-        T = (e0 - s0) // B
-        W = (T + 63) // 64
+        n = e0 - s0
+        T, C = -(-n // B), -(-n // Pg)
+        W, V = -(-T // 64), -(-C // 64)
+        unit_tile = (np.arange(-(-n // U)) * U) // B     # tile of each unit
+        unit_page = (np.arange(-(-n // U)) * U) // Pg    # page of each unit
         for h in range(Hkv):
-            M = doc_tile_masses(q, k, s0, e0, h, G, B, scale)
-            masses[(g, h)] = M
+            Mu = doc_unit_masses(q, k, s0, e0, h, G, B, U, scale)
+            M = np.zeros((T, T))
+            Mp = np.zeros((T, C))
+            for u in range(Mu.shape[1]):
+                M[:, unit_tile[u]] += Mu[:, u]
+                Mp[:, unit_page[u]] += Mu[:, u]
+            t_of = (np.arange(C) * Pg) // B
+            score = np.array([Mp[t_of[c]:, c].sum() / (T - t_of[c]) for c in range(C)])
+            masses[(g, h)], scores[(g, h)] = M, score
             lab = np.zeros((T, W * 64), bool)
             for i in range(1, T):
                 lab[i, select_top(M[i, :i], top_count(la_fraction, i))] = True
-            col = np.array([M[j:, j].sum() / (T - j) for j in range(T)])
-            cab = np.zeros(W * 64, bool)
-            cab[select_top(col, top_count(ca_fraction, T))] = True
+            cab = np.zeros(V * 64, bool)
+            cab[select_top(score, top_count(ca_fraction, C))] = True
             base = layout.la_off[g] + (layer * Hkv + h) * T * W
             la[base: base + T * W] = np.packbits(lab, axis=1, bitorder="little").view("<u8").reshape(-1)
-            cbase = layout.ca_off[g] + (layer * Hkv + h) * W
-            ca[cbase: cbase + W] = np.packbits(cab, bitorder="little").view("<u8")
-    return la, ca, masses
+            cbase = layout.ca_off[g] + (layer * Hkv + h) * V
+            ca[cbase: cbase + V] = np.packbits(cab, bitorder="little").view("<u8")
+    return la, ca, masses, scores

@@ -83,7 +83,7 @@ def test_build_bits_valid_top_and_mostly_exact(sift, case):
         torch.cuda.synchronize()
         assert int(st.item()) == 0, sift.status_string(int(st.item()))
         la_g, ca_g = _words_host(la_d), _words_host(ca_d)
-        la_o, ca_o, masses = oracle.build_bits(lay, layer, q, k, la_f, ca_f)
+        la_o, ca_o, masses, _ = oracle.build_bits(lay, layer, q, k, la_f, ca_f)
         for g, T in enumerate(tiles):
             Wd = (T + 63) // 64
             for h in range(hkv):
@@ -144,7 +144,7 @@ def test_build_bits_feeds_the_online_path(sift):
         qk.append((q, k))
         sift.build_bits(prob, layer, q, k, max(_doc_tiles(lay)), 0.3, 0.4, la_d, ca_d,
                         dev_status=st)
-        la_l, ca_l, _ = oracle.build_bits(lay, layer, q, k, 0.3, 0.4)
+        la_l, ca_l, _, _ = oracle.build_bits(lay, layer, q, k, 0.3, 0.4)
         la_o |= la_l
         ca_o |= ca_l
     torch.cuda.synchronize()

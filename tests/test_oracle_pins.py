@@ -313,7 +313,7 @@ def test_build_masses_rows_sum_to_group_rows():
                           num_q_heads=4, num_kv_heads=2, head_dim=32, tile=64)
     lay = W.make_layout(cfg)
     q, k, _ = W.make_qkv(cfg, 0)
-    _, _, masses = oracle.build_bits(lay, 0, q, k, 0.3, 0.3)
+    _, _, masses, _ = oracle.build_bits(lay, 0, q, k, 0.3, 0.3)
     for (g, h), M in masses.items():
         np.testing.assert_allclose(M.sum(axis=1), 2 * 64, rtol=1e-12)
         assert np.all(np.triu(M, 1) == 0)
@@ -326,7 +326,7 @@ def test_build_masses_match_attention_with_one_hot_values():
                           num_q_heads=2, num_kv_heads=1, head_dim=8, tile=64)
     lay = W.make_layout(cfg)
     q, k, _ = W.make_qkv(cfg, 0)
-    _, _, masses = oracle.build_bits(lay, 0, q, k, 0.5, 0.5, scale=0.2)
+    _, _, masses, _ = oracle.build_bits(lay, 0, q, k, 0.5, 0.5, scale=0.2)
     for g in range(lay.num_docs):
         s0, e0 = lay.doc_start(g), int(lay.doc_end[g])
         n = e0 - s0
@@ -357,7 +357,7 @@ def test_build_selects_planted_hot_tile():
     q = (a + 0.05 * torch.randn((512, 2, 16), generator=gen)).to(torch.bfloat16)
     k = (0.05 * torch.randn((512, 1, 16), generator=gen)).to(torch.bfloat16)
     k[2 * 64: 3 * 64, 0] = (2.0 * a).to(torch.bfloat16)          # tile 2 is hot
-    la, ca, _ = oracle.build_bits(lay, 0, q, k, 1.0 / 8, 1.0 / 8, scale=1.0)
+    la, ca, _, _ = oracle.build_bits(lay, 0, q, k, 1.0 / 8, 1.0 / 8, scale=1.0)
     for i in range(3, 8):  # rows below the hot tile keep exactly one LA tile (ceil(i/8) = 1)
         assert int(la[i]) == 1 << 2, (i, bin(int(la[i])))
     assert int(ca[0]) == 1 << 2
@@ -368,7 +368,7 @@ def test_build_counts_follow_the_fractions():
                           num_q_heads=2, num_kv_heads=1, head_dim=16, tile=64)
     lay = W.make_layout(cfg)
     q, k, _ = W.make_qkv(cfg, 0)
-    la, ca, _ = oracle.build_bits(lay, 0, q, k, 0.25, 0.4)
+    la, ca, _, _ = oracle.build_bits(lay, 0, q, k, 0.25, 0.4)
     for g, T in ((0, 20), (1, 7)):
         base = lay.la_off[g]
         for i in range(T):

@@ -317,3 +317,85 @@ def test_ragged_random_bits_match_numpy_brute_force():
     Ob, LSEb = oracle.brute_force_attention(lay, la, ca, 0, q, k, v)
     np.testing.assert_allclose(O, Ob, atol=1e-12)
     np.testing.assert_allclose(LSE, LSEb, atol=1e-12)
+
+
+# ---- the offline bit builder on the general layout -------------------------------------
+
+def test_builder_general_row_sums_and_second_route():
+    """Ragged documents, 8-token pages under 16-token tiles: each query tile's masses sum to
+    G x its rows, and the unit masses equal the oracle's own attention rows with one-hot
+    unit indicators as V (document alone)."""
+    cfg = W.custom_config("bb_rg", [([37, 50], 5)], W.BitSpec(pattern="zeros"), num_q_heads=2,
+                          num_kv_heads=1, head_dim=8, tile=16, page=8)
+    lay = W.make_layout(cfg)
+    q, k, _ = W.make_qkv(cfg, 0)
+    _, _, masses, scores = oracle.build_bits(lay, 0, q, k, 0.5, 0.5, scale=0.3)
+    for g in range(lay.num_docs):
+        s0, e0 = lay.doc_start(g), int(lay.doc_end[g])
+        n = e0 - s0
+        T = -(-n // 16)
+        rows = np.array([min(16, n - 16 * i) for i in range(T)])
+        np.testing.assert_allclose(masses[(g, 0)].sum(axis=1), 2 * rows, rtol=1e-12)
+        # second route: attention rows of the document alone with V = unit indicators
+        nu = -(-n // 8)
+        sub = W.Layout(num_prompts=1, num_docs=0, num_layers=1, num_q_heads=2, num_kv_heads=1,
+                       head_dim=8, tile=16, total_tokens=n, max_tiles_per_prompt=T,
+                       cu_seqlens=np.array([0, n], np.int32), doc_cu=np.array([0, 0], np.int32),
+                       doc_end=np.zeros(0, np.int32), la_off=np.zeros(0, np.int64),
+                       ca_off=np.zeros(0, np.int64), la_words_len=0, ca_words_len=0)
+        onehot = torch.zeros((n, 1, 8))
+        onehot[torch.arange(n), 0, torch.arange(n) // 8] = 1.0
+        tok = np.repeat(np.arange(n, dtype=np.int32), 2)
+        head = np.tile(np.arange(2, dtype=np.int32), n)
+        o, _ = oracle.attention_rows(sub, np.zeros(0, np.uint64), np.zeros(0, np.uint64), 0,
+                                     q[s0:e0], k[s0:e0], onehot.to(torch.bfloat16), tok, head,
+                                     scale=0.3)
+        per_unit = o.reshape(n, 2, 8).sum(axis=1)[:, :nu]          # [token, unit]
+        Mu = np.add.reduceat(per_unit, np.arange(0, n, 16), axis=0)  # [query tile, unit]
+        M2 = np.zeros((T, T))
+        for u in range(nu):
+            M2[:, (8 * u) // 16] += Mu[:, u]
+        np.testing.assert_allclose(masses[(g, 0)], M2, atol=1e-10)
+
+
+@pytest.mark.parametrize("page,tile,hot", [(8, 16, 5), (256, 128, 1), (16, 16, 3)])
+def test_builder_general_planted_hot_page(page, tile, hot):
+    """Keys of one page aligned with every query draw almost all the mass: it is the only
+    page CA keeps at a one-page budget, and LA rows after its tiles keep a tile of it."""
+    n = 6 * max(page, tile) + 3                       # a partial last page and tile
+    cfg = W.custom_config("bb_hot_rg", [([n], 0)], W.BitSpec(pattern="zeros"), num_q_heads=2,
+                          num_kv_heads=1, head_dim=16, tile=tile, page=page)
+    lay = W.make_layout(cfg)
+    gen = torch.Generator().manual_seed(11)
+    a = torch.randn(16, generator=gen)
+    q = (a + 0.05 * torch.randn((n, 2, 16), generator=gen)).to(torch.bfloat16)
+    k = (0.05 * torch.randn((n, 1, 16), generator=gen)).to(torch.bfloat16)
+    k[hot * page: (hot + 1) * page, 0] = (2.0 * a).to(torch.bfloat16)
+    C = lay.doc_pages(0)
+    la, ca, masses, scores = oracle.build_bits(lay, 0, q, k, 1e-3, 1.0 / C, scale=1.0)
+    assert np.argmax(scores[(0, 0)]) == hot
+    V = -(-C // 64)
+    cab = np.unpackbits(ca[:V].view(np.uint8), bitorder="little")[:C]
+    assert cab.sum() == 1 and cab[hot] == 1
+    T = lay.doc_tiles(0)
+    hot_tiles = set(range((hot * page) // tile, ((hot + 1) * page - 1) // tile + 1))
+    W_ = -(-T // 64)
+    for i in range(max(hot_tiles) + 1, T):   # one kept tile per row (ceil(1e-3 * i) = 1)
+        row = np.unpackbits(la[i * W_: (i + 1) * W_].view(np.uint8), bitorder="little")[:T]
+        assert row.sum() == 1 and int(np.nonzero(row)[0][0]) in hot_tiles, (i, row)
+
+
+def test_builder_general_counts_follow_the_fractions():
+    cfg = W.custom_config("bb_cnt_rg", [([16 * 9 + 5, 40], 7)], W.BitSpec(pattern="zeros"),
+                          num_q_heads=2, num_kv_heads=1, head_dim=8, tile=16, page=8)
+    lay = W.make_layout(cfg)
+    q, k, _ = W.make_qkv(cfg, 0)
+    la, ca, _, _ = oracle.build_bits(lay, 0, q, k, 0.3, 0.25)
+    for g in range(lay.num_docs):
+        T, C = lay.doc_tiles(g), lay.doc_pages(g)
+        W_, V = -(-T // 64), -(-C // 64)
+        for i in range(T):
+            w = la[lay.la_off[g] + i * W_: lay.la_off[g] + (i + 1) * W_]
+            assert int(sum(bin(int(x)).count("1") for x in w)) == int(np.ceil(0.3 * i - 1e-4))
+        w = ca[lay.ca_off[g]: lay.ca_off[g] + V]
+        assert int(sum(bin(int(x)).count("1") for x in w)) == int(np.ceil(0.25 * C - 1e-4))
