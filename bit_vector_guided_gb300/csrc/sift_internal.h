@@ -27,6 +27,14 @@ sift_status validate_ragged(const sift_problem *p, bool attention);
 // upper bound on the per-segment query tiles: ceil(tokens/tile) + documents + prompts
 int64_t max_query_tiles(const sift_problem *p);
 
+// sift_decode_ragged with `exact` = false: num_query_tiles is an upper bound, the rows past
+// the real count get an empty query tile (computed, never stored)
+sift_status decode_ragged_impl(const sift_problem *prob, int32_t num_query_tiles,
+                               const uint64_t *la_words, const uint64_t *ca_words,
+                               int32_t *qtiles, int32_t *kv, int32_t *counts, int32_t *sched,
+                               int32_t *pages, int32_t page_cap, int32_t *dev_status,
+                               cudaStream_t stream, bool exact);
+
 // general layout: CA pages below the tile (and a multiple of 8 tokens) are gathered
 // into dense tiles rather than masked inside contiguous ones
 inline bool gathers_pages(const sift_problem *p) {

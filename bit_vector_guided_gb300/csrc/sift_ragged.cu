@@ -31,9 +31,10 @@ struct RaggedArgs {
     int64_t la_len, ca_len;
     int32_t *qt, *kv, *counts, *status;
     int32_t *pages;  // gathered pages [L][Hkv][D][page_cap] (gather only)
-    int P, D, Hkv, L, B, page, NQ, rowcap, page_cap;
+    int P, D, Hkv, L, B, page, NQ, rowcap, page_cap, T;
     uint32_t full;   // mask bits of a tile with every page kept
     bool gather;     // page < tile and a multiple of 8: CA pages are gathered into tiles
+    bool exact;      // NQ is the exact tile count (else an upper bound; spare rows stay empty)
 };
 
 __device__ __forceinline__ void rstatus(int32_t *st, int code) { atomicCAS(st, 0, code); }
@@ -117,16 +118,19 @@ __global__ void __launch_bounds__(1024) ragged_tiles_kernel(RaggedArgs a) {
         __syncthreads();
     }
     const int total = carry;
-    if (tid == 0 && total != a.NQ) rstatus(a.status, SIFT_ERR_DEVICE_CHECK);
-    // rows the segments did not fill (only after an inconsistency): one empty query tile
-    // with a one-entry list, so that every row the attention kernel reads is defined
+    if (tid == 0 && (a.exact ? total != a.NQ : total > a.NQ))
+        rstatus(a.status, SIFT_ERR_DEVICE_CHECK);
+    // rows the segments did not fill (a row count given as an upper bound, or an
+    // inconsistency): an empty query tile at the end of the batch -- which keeps the table
+    // ascending -- with a one-entry list, so that every row the attention kernel reads is
+    // defined (its loads fall past the tensors and read zeros; nothing is stored)
     for (int q = total + tid; q < a.NQ; q += 1024) {
-        a.qt[2 * q] = 0;
+        a.qt[2 * q] = a.T;
         a.qt[2 * q + 1] = 0;
         for (int lh = 0; lh < a.L * a.Hkv; ++lh) {
             const int64_t row = static_cast<int64_t>(lh) * a.NQ + q;
             a.counts[row] = 1;
-            a.kv[2 * row * a.rowcap] = 0;
+            a.kv[2 * row * a.rowcap] = a.T;
             a.kv[2 * row * a.rowcap + 1] = static_cast<int32_t>(1u | 1u << 8 | a.full << 16);
         }
     }
@@ -349,12 +353,13 @@ __global__ void __launch_bounds__(kRaggedWarps * 32) ragged_decode_kernel(Ragged
 }  // namespace
 }  // namespace sift
 
-extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles,
-                                          const uint64_t *la_words, const uint64_t *ca_words,
-                                          int32_t *qtiles, int32_t *kv, int32_t *counts,
-                                          int32_t *sched, int32_t *pages, int32_t page_cap,
-                                          int32_t *dev_status, cudaStream_t stream) {
-    using namespace sift;
+namespace sift {
+
+sift_status decode_ragged_impl(const sift_problem *prob, int32_t num_query_tiles,
+                               const uint64_t *la_words, const uint64_t *ca_words,
+                               int32_t *qtiles, int32_t *kv, int32_t *counts, int32_t *sched,
+                               int32_t *pages, int32_t page_cap, int32_t *dev_status,
+                               cudaStream_t stream, bool exact) {
     sift_status st = validate_ragged(prob, false);
     if (st != SIFT_OK) return st;
     if (num_query_tiles < 1 || num_query_tiles > max_query_tiles(prob)) return SIFT_ERR_INVALID_ARG;
@@ -393,9 +398,11 @@ extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_
     a.B = prob->tile;
     a.page = prob->page ? prob->page : prob->tile;
     a.NQ = num_query_tiles;
+    a.T = prob->total_tokens;
     a.rowcap = prob->max_tiles_per_prompt;
     const int pin = a.page < a.B ? a.page : a.B;
     a.full = (1u << (a.B / pin)) - 1u;
+    a.exact = exact;
     ragged_tiles_kernel<<<1, 1024, 0, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SIFT_ERR_CUDA;
     const int64_t warps = static_cast<int64_t>(a.L) * a.Hkv * (a.D + a.P);
@@ -407,4 +414,15 @@ extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_
         cudaSuccess)
         return SIFT_ERR_CUDA;
     return SIFT_OK;
+}
+
+}  // namespace sift
+
+extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles,
+                                          const uint64_t *la_words, const uint64_t *ca_words,
+                                          int32_t *qtiles, int32_t *kv, int32_t *counts,
+                                          int32_t *sched, int32_t *pages, int32_t page_cap,
+                                          int32_t *dev_status, cudaStream_t stream) {
+    return sift::decode_ragged_impl(prob, num_query_tiles, la_words, ca_words, qtiles, kv,
+                                    counts, sched, pages, page_cap, dev_status, stream, true);
 }

@@ -216,17 +216,22 @@ sift_status sift_dense_prefill_noalloc(const sift_problem *prob, const void *q, 
  * Offline construction of one layer's LA and CA bit vectors (SIFT pages,
  * "Design del Sistema": each document is prefilled densely on its own once,
  * the tiles and pages that draw high attention are found and stored as bits).
- * The pages name no selection rule; this library's rule, per document, kv head
- * h and the document's own tiles (T of them):
- *   - tile mass M[i][j] = sum over the query heads of h's group and the B rows
- *     of query tile i of the attention probability on the keys of tile j, from
- *     a causal prefill of the document alone (j <= i);
+ * Works on both layouts: aligned, and documents of any length with CA pages
+ * of their own size (tiles and pages counted from each document's first
+ * token, the last ones partial).  The pages name no selection rule; this
+ * library's rule, per document, kv head h, T tiles and C pages:
+ *   - masses are gathered per unit of min(page, tile) tokens from a causal
+ *     prefill of the document alone: the attention probability that the rows
+ *     of query tile i, over the query heads of h's group, put on each unit;
+ *   - tile mass M[i][j] = the mass of tile j's units;
  *   - LA row i: the top ceil(la_fraction * i - 1e-4) tiles j < i by M[i][j]
  *     (the diagonal is implicit and never written; bits at j >= i are zero);
- *   - CA: the top ceil(ca_fraction * T - 1e-4) pages j by the mean mass they
- *     receive, sum over i >= j of M[i][j] / (T - j);
+ *   - CA: the top ceil(ca_fraction * C - 1e-4) pages by score(c) = sum over
+ *     query tiles i >= t(c) of the mass on page c, over (T - t(c)), where t(c)
+ *     is the tile of page c's first token (page == tile: the mean mass that
+ *     tile j receives from the rows i >= j);
  *   - counts in float32 with each operation rounded on its own; ties go to
- *     the lower index; masses come from the bf16 dense kernel, so tiles of
+ *     the lower index; masses come from the bf16 attention kernel, so tiles of
  *     nearly equal mass may swap against an exact computation.
  *   prob:           the attention problem (device arrays as for sift_decode);
  *                   its la_off, ca_off, la_words_len, ca_words_len say where
@@ -234,8 +239,8 @@ sift_status sift_dense_prefill_noalloc(const sift_problem *prob, const void *q, 
  *                   prompt's own rows in q and k
  *   layer:          which layer's words to write (q and k are that layer's)
  *   q, k:           bf16 [total_tokens][heads][head_dim], as for the prefill
- *   max_doc_tiles:  upper bound on any document's tile count (1 ..
- *                   max_tiles_per_prompt); sizes the workspace
+ *   max_doc_tiles:  upper bound on any document's tiles, ceil(length/tile)
+ *                   (1 .. max_tiles_per_prompt); sizes the workspace
  *   la_fraction, ca_fraction: in [0, 1]
  *   softmax_scale:  0 selects 1/sqrt(head_dim)
  *   la_words, ca_words: device, written only at this layer's blocks
@@ -243,8 +248,7 @@ sift_status sift_dense_prefill_noalloc(const sift_problem *prob, const void *q, 
  * A document longer than max_doc_tiles, or offsets outside the word arrays,
  * set SIFT_ERR_DEVICE_CHECK in dev_status; those words are not written.  A
  * batch without documents returns SIFT_OK and enqueues nothing.
- * Launches: 1 + ceil(max_doc_tiles / head_dim) x (2 + the three of
- * sift_dense_prefill) + 1.
+ * Launches: 4 + ceil(units of the longest document / head_dim) x 3 + 2.
  */
 size_t sift_build_bits_workspace_bytes(const sift_problem *prob, int32_t max_doc_tiles);
 sift_status sift_build_bits(const sift_problem *prob, int32_t layer, const void *q, const void *k,
