@@ -298,6 +298,13 @@ __device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&r)[64
         : "memory");
 }
 
+// 32-byte global store (one whole sector); the address must be 32-byte aligned
+__device__ __forceinline__ void st_global_v8(void *ptr, const uint32_t *r) {
+    asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(ptr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- packed fp32 (two lanes per op)
 __device__ __forceinline__ uint64_t f2(float lo, float hi) {
     uint64_t r;

@@ -119,6 +119,7 @@ struct AttnParams {
     const int32_t *pages;    // gathered pages: layer slice [Hkv][D][page_cap] of first tokens
     int64_t pages_len;       // entries in that slice
     int32_t page;            // page size in tokens (gathered loads are page rows high)
+    int32_t o_v8;            // o is 32-byte aligned: the epilogue writes whole sectors
 };
 
 constexpr uint32_t kGatherBit = 1u << 9;  // list entry of gathered pages (general layout)
@@ -957,10 +958,15 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     for (int t = 0; t < 16; ++t)
                         pk[t] = ptx::pack_bf16x2(ov[2 * t] * inv, ov[2 * t + 1] * inv);
                     if (store) {
+                        if (p.o_v8) {  // whole 32-byte sectors: half the store instructions
+                            ptx::st_global_v8(orow + cc * 4, pk);
+                            ptx::st_global_v8(orow + cc * 4 + 2, pk + 8);
+                        } else {
 #pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            orow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1],
-                                                           pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                            for (int v4 = 0; v4 < 4; ++v4)
+                                orow[cc * 4 + v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1],
+                                                               pk[4 * v4 + 2], pk[4 * v4 + 3]);
+                        }
                     }
                 }
                 if (store)
@@ -1078,6 +1084,7 @@ sift_status prepare(const sift_problem *prob, const void *q, const void *k, cons
     const int G = prob->num_q_heads / prob->num_kv_heads;
     AttnParams a{};
     a.o = static_cast<__nv_bfloat16 *>(o);
+    a.o_v8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     a.lse = lse;
     a.work_counter = static_cast<int32_t *>(workspace);
     a.status = dev_status;
