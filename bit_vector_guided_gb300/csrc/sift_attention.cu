@@ -80,7 +80,9 @@ struct WorkItem {
 };
 
 struct Ctl {
-    uint64_t q_full, q_empty;
+    // per head slot: a slot's Q for the next item loads as soon as this item's last S of
+    // that head is done (head 0's a step before head 1's)
+    uint64_t q_full[2], q_empty[2];
     uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots], v_empty[kVSlots];
     uint64_t s_full[2], p_full[2], o_full[2];
     uint64_t sch_full[2], sch_empty[2];
@@ -488,8 +490,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     auto B_ = [&](const uint64_t &b) { return ptx::smem_u32(&b); };
 
     if (threadIdx.x == 0) {
-        ptx::mbar_init(B_(c.q_full), 1);
-        ptx::mbar_init(B_(c.q_empty), 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(B_(c.q_full[s]), 1);
+            ptx::mbar_init(B_(c.q_empty[s]), 1);
+        }
         for (int s = 0; s < kKSlots; ++s) {
             ptx::mbar_init(B_(c.k_full[s]), 1);
             ptx::mbar_init(B_(c.k_empty[s]), 1);
@@ -647,6 +651,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     } else if (warp == kVProducerWarp) {
         // ------------------------------------------------ Q + V producer (runs behind the K producer)
         int item_k = 0, vf = 0, qk = 0;
+        int q_issued[2] = {0, 0};  // Q loads issued per head slot (drained on abort)
         bool alive = true;
         const uint64_t pol_kv = ptx::policy_evict_last();
         const uint64_t pol_q = ptx::policy_evict_first();   // Q is read once per item
@@ -658,15 +663,22 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             if (lane == 0) ptx::mbar_arrive(B_(c.sch_empty[slot]));
             ++item_k;
             if (!it.valid) break;
-            if (!wait_warp(c, B_(c.q_empty), (qk & 1) ^ 1, p)) break;
-            if (lane == 0) {
-                ptx::mbar_arrive_expect_tx(B_(c.q_full), G::kTxQ);
-                for (int s = 0; s < 2; ++s)
+            bool q_ok = true;
+            for (int s = 0; s < 2 && q_ok; ++s) {
+                if (!wait_warp(c, B_(c.q_empty[s]), (qk & 1) ^ 1, p)) {
+                    q_ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(B_(c.q_full[s]), G::kTxQ / 2);
                     for (int b = 0; b < G::kBoxes; ++b)
                         ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
-                                              B_(c.q_full), 64 * b, it.hq0 + s,
+                                              B_(c.q_full[s]), 64 * b, it.hq0 + s,
                                               RAGGED ? it.q0 : it.i * BT, pol_q);
+                }
+                ++q_issued[s];
             }
+            if (!q_ok) break;
             ++qk;
             auto load_v = [&](int idx) -> bool {
                 const int vs = vf % kVSlots;
@@ -730,7 +742,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const int last = s + ((vf - 1 - s) / kVSlots) * kVSlots;
                 drain_bar(B_(c.v_full[s]), (last / kVSlots) & 1, p.timeout_ns);
             }
-            if (qk > 0) drain_bar(B_(c.q_full), (qk - 1) & 1, p.timeout_ns);
+            for (int s = 0; s < 2; ++s)
+                if (q_issued[s] > 0) drain_bar(B_(c.q_full[s]), (q_issued[s] - 1) & 1, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
@@ -782,7 +795,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 ptx::mbar_arrive(B_(c.sch_empty[slot]));
                 ++item_k;
                 if (!it.valid) break;
-                if (!wait1(c, B_(c.q_full), qk & 1, p)) break;
+                const uint32_t qph = qk & 1;
+                if (!wait1(c, B_(c.q_full[0]), qph, p)) break;
                 ++qk;
                 ptx::tc_fence_after();
                 bool ok = true;
@@ -806,6 +820,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         pph1 ^= 1;
                         ptx::tc_fence_after();
                         issue_pv(1, vs, j > 1);
+                    }
+                    if (j == 0) {  // head 1's Q of this item
+                        if (!wait1(c, B_(c.q_full[1]), qph, p)) { ok = false; break; }
+                        ptx::tc_fence_after();
                     }
                     issue_s(1, ks);
                     ptx::umma_commit(B_(c.s_full[1]));
@@ -848,6 +866,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             // last MMA to read K_j and Q (at the item's last tile), and completes after
             // PV1(j-1), the last reader of V_{j-1}; o_full of slot 1 covers the item's last V.
             const bool releaser = (s == 1 && wq == 0 && lane == 0);
+            // and the first warp of head slot 0 hands back that slot's Q after its last S
+            const bool q0_releaser = (s == 0 && wq == 0 && lane == 0);
             int t = 0;  // key tiles seen so far, same order as the producers and the MMA issuer
             while (true) {
                 const int slot = item_k & 1;
@@ -868,8 +888,9 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     if (releaser) {
                         ptx::mbar_arrive(B_(c.k_empty[t % kKSlots]));
                         if (j > 0) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
-                        if (j == it.n - 1) ptx::mbar_arrive(B_(c.q_empty));
+                        if (j == it.n - 1) ptx::mbar_arrive(B_(c.q_empty[1]));
                     }
+                    if (q0_releaser && j == it.n - 1) ptx::mbar_arrive(B_(c.q_empty[0]));
                     ++t;
                     ptx::tc_fence_after();
                     float x[BT];
