@@ -581,13 +581,14 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             auto load_k = [&](int idx) -> bool {
                 const int ks = kf % kKSlots;
                 if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
-                    for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox, &tmK,
-                                              B_(c.k_full[ks]), 64 * b, it.h,
-                                              RAGGED ? idx : idx * BT, pol_kv);
-                }
+                // lane 0 registers the bytes, then each box is issued by its own lane (a
+                // thread issues bulk tensor copies slowly one after another)
+                if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
+                __syncwarp();
+                if (static_cast<int>(lane) < G::kBoxes)
+                    ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + lane * G::kKVBox, &tmK,
+                                          B_(c.k_full[ks]), 64 * lane, it.h,
+                                          RAGGED ? idx : idx * BT, pol_kv);
                 ++kf;
                 return true;
             };
@@ -606,16 +607,14 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const int ks = kf % kKSlots;
                 if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.k_full[ks]), G::kTxKV);
+                __syncwarp();
+                // one box per lane: lane = slot * boxes + box (at most 16 slots x 2 boxes)
                 const int per = BT / p.page;
-                for (int sl = 0; sl < per; ++sl) {
-                    const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
-                    if (lane == 0)
-                        for (int b = 0; b < G::kBoxes; ++b)
-                            ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox +
-                                                      sl * p.page * 128,
-                                                  &tmKp, B_(c.k_full[ks]), 64 * b, it.h, pst,
-                                                  pol_kv);
-                }
+                const int sl = static_cast<int>(lane) / G::kBoxes, b = static_cast<int>(lane) % G::kBoxes;
+                const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
+                if (sl < per)
+                    ptx::tma_load_3d_hint(k_s + ks * G::kKVBytes + b * G::kKVBox + sl * p.page * 128,
+                                          &tmKp, B_(c.k_full[ks]), 64 * b, it.h, pst, pol_kv);
                 ++kf;
                 return true;
             };
@@ -669,13 +668,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     q_ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(B_(c.q_full[s]), G::kTxQ / 2);
-                    for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + b) * G::kQBox, &tmQ,
-                                              B_(c.q_full[s]), 64 * b, it.hq0 + s,
-                                              RAGGED ? it.q0 : it.i * BT, pol_q);
-                }
+                if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.q_full[s]), G::kTxQ / 2);
+                __syncwarp();
+                if (static_cast<int>(lane) < G::kBoxes)
+                    ptx::tma_load_3d_hint(q_s + (s * G::kBoxes + lane) * G::kQBox, &tmQ,
+                                          B_(c.q_full[s]), 64 * lane, it.hq0 + s,
+                                          RAGGED ? it.q0 : it.i * BT, pol_q);
                 ++q_issued[s];
             }
             if (!q_ok) break;
@@ -683,13 +681,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             auto load_v = [&](int idx) -> bool {
                 const int vs = vf % kVSlots;
                 if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) return false;
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
-                    for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox, &tmV,
-                                              B_(c.v_full[vs]), 64 * b, it.h,
-                                              RAGGED ? idx : idx * BT, pol_kv);
-                }
+                if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
+                __syncwarp();
+                if (static_cast<int>(lane) < G::kBoxes)
+                    ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + lane * G::kKVBox, &tmV,
+                                          B_(c.v_full[vs]), 64 * lane, it.h,
+                                          RAGGED ? idx : idx * BT, pol_kv);
                 ++vf;
                 return true;
             };
@@ -703,16 +700,13 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const int vs = vf % kVSlots;
                 if (!wait_warp(c, B_(c.v_empty[vs]), ((vf / kVSlots) & 1) ^ 1, p)) return false;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(B_(c.v_full[vs]), G::kTxKV);
+                __syncwarp();
                 const int per = BT / p.page;
-                for (int sl = 0; sl < per; ++sl) {
-                    const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
-                    if (lane == 0)
-                        for (int b = 0; b < G::kBoxes; ++b)
-                            ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox +
-                                                      sl * p.page * 128,
-                                                  &tmVp, B_(c.v_full[vs]), 64 * b, it.h, pst,
-                                                  pol_kv);
-                }
+                const int sl = static_cast<int>(lane) / G::kBoxes, b = static_cast<int>(lane) % G::kBoxes;
+                const int pst = __shfl_sync(kFull, ps, sl < np ? sl : 0);
+                if (sl < per)
+                    ptx::tma_load_3d_hint(v_s + vs * G::kKVBytes + b * G::kKVBox + sl * p.page * 128,
+                                          &tmVp, B_(c.v_full[vs]), 64 * b, it.h, pst, pol_kv);
                 ++vf;
                 return true;
             };
