@@ -58,3 +58,43 @@ def test_shards_match_unsharded(sift, world):
             assert torch.equal(o_s, o[:, h0 * G:h1 * G]) and torch.equal(o_f, o_s)
             assert torch.equal(lse_s, lse[h0 * G:h1 * G]) and torch.equal(lse_f, lse_s)
         assert int(st.item()) == 0
+
+
+@pytest.mark.parametrize("world", [2, 4])
+def test_general_layout_shards_match_unsharded(sift, world):
+    """Ragged documents with 16-token pages gathered: each shard's general-layout prefill
+    equals the head slice of the unsharded one, bit for bit."""
+    cfg = W.custom_config("shard_gpu_rg", [([300, 411, 77], 50), ([190], 0)],
+                          W.BitSpec(la_p=0.4, ca_p=0.3), num_layers=1, num_q_heads=16,
+                          num_kv_heads=4, head_dim=128, tile=128, page=16)
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, "cuda")
+    la_d, ca_d = device_bits(la, ca)
+    st = prob.new_status()
+    lists = sift.decode_ragged(prob, la_d, ca_d, dev_status=st)
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    o, lse = sift.sparse_prefill_ragged(prob, 0, q, k, v, *lists, dev_status=st)
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    for r in range(world):
+        h0, h1 = kv_head_range(r, world, cfg.num_kv_heads)
+        la_off, ca_off, la_s, ca_s = shard_bits(lay.cu_seqlens, lay.doc_cu, lay.doc_end,
+                                                lay.la_off, lay.ca_off, la, ca, cfg.num_layers,
+                                                cfg.num_kv_heads, cfg.tile, h0, h1, page=16)
+        sp = sift.SiftProblem(cu_seqlens=lay.cu_seqlens, doc_cu=lay.doc_cu, doc_end=lay.doc_end,
+                              la_off=la_off, ca_off=ca_off, num_layers=cfg.num_layers,
+                              num_q_heads=(h1 - h0) * G, num_kv_heads=h1 - h0,
+                              head_dim=cfg.head_dim, tile=cfg.tile, la_words_len=len(la_s),
+                              ca_words_len=len(ca_s), max_tiles_per_prompt=lay.max_tiles_per_prompt,
+                              page=16)
+        las, cas = device_bits(la_s, ca_s)
+        ss = sp.new_status()
+        lists_s = sift.decode_ragged(sp, las, cas, dev_status=ss)
+        qs = q[:, h0 * G:h1 * G].contiguous()
+        ks, vs = k[:, h0:h1].contiguous(), v[:, h0:h1].contiguous()
+        o_s, lse_s = sift.sparse_prefill_ragged(sp, 0, qs, ks, vs, *lists_s, dev_status=ss)
+        torch.cuda.synchronize()
+        assert int(ss.item()) == 0
+        assert torch.equal(o_s, o[:, h0 * G:h1 * G])
+        assert torch.equal(lse_s, lse[h0 * G:h1 * G])
+    assert int(st.item()) == 0

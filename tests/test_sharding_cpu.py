@@ -32,6 +32,47 @@ def shard_layout(lay, la, ca, h0, h1):
     return sub, la_s, ca_s
 
 
+RG = W.custom_config("shard_cpu_rg", [([250, 513, 77], 45), ([190], 0), ([], 30)],
+                     W.BitSpec(la_p=0.4, ca_p=0.3), num_layers=2, num_q_heads=12,
+                     num_kv_heads=6, head_dim=64, tile=64, page=8)
+
+
+@pytest.mark.parametrize("world", [2, 3, 6])
+def test_general_layout_shards_decode_to_the_head_slices(world):
+    """Ragged documents, 8-token pages (gathered): each shard's re-packed words decode to
+    the head slice of the unsharded lists, page starts included."""
+    lay = W.make_layout(RG)
+    la, ca = W.make_bits(RG, lay)
+    qt, kv, cnt, pg = oracle.decode_ragged(lay, la, ca)
+    G = lay.num_q_heads // lay.num_kv_heads
+    for r in range(world):
+        h0, h1 = kv_head_range(r, world, lay.num_kv_heads)
+        la_off, ca_off, la_s, ca_s = shard_bits(lay.cu_seqlens, lay.doc_cu, lay.doc_end,
+                                                lay.la_off, lay.ca_off, la, ca, lay.num_layers,
+                                                lay.num_kv_heads, lay.tile, h0, h1, page=8)
+        import dataclasses
+        sub = dataclasses.replace(lay, num_q_heads=(h1 - h0) * G, num_kv_heads=h1 - h0,
+                                  la_off=la_off, ca_off=ca_off, la_words_len=len(la_s),
+                                  ca_words_len=len(ca_s))
+        qt_s, kv_s, cnt_s, pg_s = oracle.decode_ragged(sub, la_s, ca_s)
+        assert np.array_equal(qt_s, qt)
+        assert np.array_equal(cnt_s, cnt[:, h0:h1])
+        H = h1 - h0
+        for l in range(lay.num_layers):
+            for hh in range(H):
+                for q in range(len(qt)):
+                    n = cnt_s[l, hh, q]
+                    for (f, info), (f0, info0) in zip(kv_s[l, hh, q, :n], kv[l, h0 + hh, q, :n]):
+                        assert info == info0
+                        if (int(info) >> 9) & 1:   # gathered: compare the pages themselves
+                            npg = (int(info) & 0xFF) // 8
+                            a = pg_s[l].reshape(-1)[f: f + npg]
+                            b = pg[l].reshape(-1)[f0: f0 + npg]
+                            assert np.array_equal(a, b)
+                        else:
+                            assert f == f0
+
+
 @pytest.mark.parametrize("world", [1, 2, 3, 4, 6])
 def test_shards_decode_to_the_head_slices(world):
     lay = W.make_layout(CFG)
