@@ -200,3 +200,44 @@ def test_ragged_full_size_workload(sift):
         lg = lse[torch.as_tensor(head, device="cuda").long(),
                  torch.as_tensor(tok, device="cuda").long()].double().cpu().numpy()
         assert_attention_close(og, lg, O, LSE, f"ragged 33K layer {layer}")
+
+
+def test_ragged_decode_many_segments_and_prompts(sift):
+    """More than 1024 segments (the query-tile scan then runs over several chunks with a
+    carry) spread over 350 prompts: decode bit-exact against the oracle."""
+    rng = np.random.default_rng(3)
+    prompts = []
+    for p in range(350):
+        docs = [int(x) for x in rng.integers(1, 40, size=int(rng.integers(0, 6)))]
+        prompts.append((docs, int(rng.integers(0, 3) * 7)))
+    cfg = W.custom_config("rg_many", prompts, W.BitSpec(la_p=0.4, ca_p=0.4), num_layers=1,
+                          num_q_heads=2, num_kv_heads=1, head_dim=64, tile=64, page=16)
+    lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
+    assert lay.num_docs + lay.num_prompts > 1024
+    _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
+
+
+def test_ragged_decode_reports_a_wrong_tile_count(sift):
+    """A query-tile count that disagrees with the segments is reported on the device; the
+    spare row becomes an empty tile past the end of the batch."""
+    import ctypes
+    cfg = CFGS[0]
+    lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
+    NQ = prob.num_query_tiles + 1
+    L, H, R = cfg.num_layers, cfg.num_kv_heads, prob.max_tiles_per_prompt
+    qt = torch.empty((NQ, 2), dtype=torch.int32, device="cuda")
+    kv = torch.empty((L, H, NQ, R, 2), dtype=torch.int32, device="cuda")
+    cnt = torch.empty((L, H, NQ), dtype=torch.int32, device="cuda")
+    sch = torch.empty((L, H * NQ), dtype=torch.int32, device="cuda")
+    pages = torch.empty((L, H, lay.num_docs, prob.page_cap), dtype=torch.int32, device="cuda")
+    st = prob.new_status()
+    lib = sift.load_library()
+    rc = lib.sift_decode_ragged(prob.ref, NQ, la_d.data_ptr(), ca_d.data_ptr(), qt.data_ptr(),
+                                kv.data_ptr(), cnt.data_ptr(), sch.data_ptr(), pages.data_ptr(),
+                                prob.page_cap, st.data_ptr(),
+                                torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(st.item()) == 5  # SIFT_ERR_DEVICE_CHECK
+    assert qt[NQ - 1].tolist() == [lay.total_tokens, 0]
+    assert cnt[:, :, NQ - 1].eq(1).all()
