@@ -92,9 +92,9 @@ def kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(path=PROFILE_SUMMARY):
+def profiled_traffic(path, workload):
     """DRAM bytes per launch of the sparse kernel from a committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+    taken on the current kernel source and on this workload (else None)."""
     if not os.path.exists(path):
         return None
     vals = {}
@@ -104,6 +104,8 @@ def profiled_traffic(path=PROFILE_SUMMARY):
                 k, _, v = line.strip()[2:].partition(":")
                 vals[k.strip()] = v.strip().strip("`")
     if vals.get("kernel_source_sha256_16") != kernel_source_digest():
+        return None
+    if vals.get("workload") != workload:
         return None
     try:
         return float(vals["traffic_bytes_per_launch"])
@@ -400,7 +402,7 @@ def run_ours(args, cfg):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = profiled_traffic()
+    traffic = None if shard else profiled_traffic(PROFILE_SUMMARY, cfg.name)
 
     # decode fused into the prefill: the same step without a separate decode
     fz0, fz1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -785,7 +787,7 @@ def run_ragged_line(args, cfg):
         "data": "synthetic", "config": config_dict(cfg, args, lay),
         "roofline": {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
                      "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak,
-                     "traffic": profiled_traffic(PROFILE_RAGGED),
+                     "traffic": profiled_traffic(PROFILE_RAGGED, cfg.name),
                      "kernel": "sift_sparse_prefill_ragged",
                      "peak_source": f"bf16_tflops_sustained of {peak_src}"},
         "gpu_launches": args.steps * r["gpu_launches_per_step"], "ragged": r,
