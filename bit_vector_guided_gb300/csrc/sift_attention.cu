@@ -741,12 +741,17 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         __syncwarp();
     } else if (warp == kMmaWarp) {
-        // ------------------------------------------------ single-thread MMA issuer
-        // One thread issues both heads' MMAs in the order S0(j) | PV1(j-1) S1(j) |
+        // ------------------------------------------------ MMA issuer warp
+        // Both heads' MMAs are issued in the order S0(j) | PV1(j-1) S1(j) |
         // PV0(j) S0(j+1) | ...: the heads alternate on the tensor pipe, each one's softmax
         // running while the other head's MMAs execute.
-        if (lane == 0) {
-            if (p.stall) wait_bar(c, B_(c.never), 0, p.timeout_ns, p.status);
+        {
+            // The whole warp runs the issue loop on warp-uniform values (ring positions,
+            // descriptors, waits made uniform by the vote) and one elected lane issues each
+            // MMA and commit.  Run by a single lane, the loop lost about 7% end to end: its
+            // operands first had to leave that lane's registers, on a sub-partition shared
+            // with two busy softmax warps.
+            if (p.stall) (void)wait_warp(c, B_(c.never), 0, p);
             int item_k = 0, qk = 0;
             // ring positions kept incrementally (no division on the issue path): K slot and
             // phase of the current tile, V slot and phase of the previous tile
@@ -760,46 +765,55 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             const uint64_t dq = ptx::sdesc_sw128(q_s, 16, 1024);
             const uint64_t dk = ptx::sdesc_sw128(k_s, 16, 1024);
             const uint64_t dv = ptx::sdesc_sw128(v_s, G::kKVBox, 1024);
+            auto commit = [&](uint32_t bar) {
+                if (ptx::elect_one()) ptx::umma_commit(bar);
+            };
             auto issue_s = [&](int s, int kslot) {
                 const uint64_t qa = dq + static_cast<uint32_t>((s * G::kBoxes * G::kQBox) >> 4);
                 const uint64_t kb = dk + static_cast<uint32_t>((kslot * G::kKVBytes) >> 4);
                 const uint32_t d = s ? tS1 : tS0;
-                ptx::umma_ss_c<false>(d, qa, kb, G::kIdescS);
+                if (ptx::elect_one()) ptx::umma_ss_c<false>(d, qa, kb, G::kIdescS);
 #pragma unroll
                 for (int kk = 1; kk < HD / 16; ++kk) {
                     const uint32_t off_q = ((kk >> 2) * G::kQBox + (kk & 3) * 32) >> 4;
                     const uint32_t off_k = ((kk >> 2) * G::kKVBox + (kk & 3) * 32) >> 4;
-                    ptx::umma_ss_c<true>(d, qa + off_q, kb + off_k, G::kIdescS);
+                    if (ptx::elect_one()) ptx::umma_ss_c<true>(d, qa + off_q, kb + off_k, G::kIdescS);
                 }
             };
             auto issue_pv = [&](int s, int vslot, bool acc) {
                 const uint64_t vb = dv + static_cast<uint32_t>((vslot * G::kKVBytes) >> 4);
                 const uint32_t d = s ? tO1 : tO0;
                 const uint32_t a = s ? tS1 : tS0;
-                if (acc) ptx::umma_ts_c<true>(d, a, vb, G::kIdescPV);
-                else ptx::umma_ts_c<false>(d, a, vb, G::kIdescPV);
+                if (ptx::elect_one()) {
+                    if (acc) ptx::umma_ts_c<true>(d, a, vb, G::kIdescPV);
+                    else ptx::umma_ts_c<false>(d, a, vb, G::kIdescPV);
+                }
 #pragma unroll
                 for (int kk = 1; kk < BT / 16; ++kk)
-                    ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
+                    if (ptx::elect_one())
+                        ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
             };
-            while (!c.abort) {
+            while (__shfl_sync(kFull, c.abort, 0) == 0) {  // one read for the whole warp
                 const int slot = item_k & 1;
-                if (!wait1(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
-                const WorkItem it = c.items[slot];
-                ptx::mbar_arrive(B_(c.sch_empty[slot]));
+                if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
+                // the item's tile count, uniform across the warp
+                const int valid = __shfl_sync(kFull, c.items[slot].valid, 0);
+                const int n_tiles = __shfl_sync(kFull, c.items[slot].n, 0);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(B_(c.sch_empty[slot]));
                 ++item_k;
-                if (!it.valid) break;
+                if (!valid) break;
                 const uint32_t qph = qk & 1;
-                if (!wait1(c, B_(c.q_full[0]), qph, p)) break;
+                if (!wait_warp(c, B_(c.q_full[0]), qph, p)) break;
                 ++qk;
                 ptx::tc_fence_after();
                 bool ok = true;
-                for (int j = 0; j < it.n; ++j) {
-                    if (!wait1(c, B_(c.k_full[ks]), kph, p)) { ok = false; break; }
+                for (int j = 0; j < n_tiles; ++j) {
+                    if (!wait_warp(c, B_(c.k_full[ks]), kph, p)) { ok = false; break; }
                     ptx::tc_fence_after();
                     if (j > 0) {
-                        if (!wait1(c, B_(c.v_full[vs]), vph, p) ||
-                            !wait1(c, B_(c.p_full[0]), pph0, p)) {
+                        if (!wait_warp(c, B_(c.v_full[vs]), vph, p) ||
+                            !wait_warp(c, B_(c.p_full[0]), pph0, p)) {
                             ok = false;
                             break;
                         }
@@ -808,39 +822,39 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         issue_pv(0, vs, j > 1);
                     }
                     issue_s(0, ks);
-                    ptx::umma_commit(B_(c.s_full[0]));
+                    commit(B_(c.s_full[0]));
                     if (j > 0) {
-                        if (!wait1(c, B_(c.p_full[1]), pph1, p)) { ok = false; break; }
+                        if (!wait_warp(c, B_(c.p_full[1]), pph1, p)) { ok = false; break; }
                         pph1 ^= 1;
                         ptx::tc_fence_after();
                         issue_pv(1, vs, j > 1);
                     }
                     if (j == 0) {  // head 1's Q of this item
-                        if (!wait1(c, B_(c.q_full[1]), qph, p)) { ok = false; break; }
+                        if (!wait_warp(c, B_(c.q_full[1]), qph, p)) { ok = false; break; }
                         ptx::tc_fence_after();
                     }
                     issue_s(1, ks);
-                    ptx::umma_commit(B_(c.s_full[1]));
+                    commit(B_(c.s_full[1]));
                     // advance: this tile's V becomes "previous", the K ring moves on
                     if (++vs == kVSlots) { vs = 0; vph ^= 1; }
                     if (++ks == kKSlots) { ks = 0; kph ^= 1; }
                 }
                 if (!ok) break;
                 // vs / vph now name the item's last V tile
-                if (!wait1(c, B_(c.v_full[vs]), vph, p)) break;
-                if (!wait1(c, B_(c.p_full[0]), pph0, p)) break;
+                if (!wait_warp(c, B_(c.v_full[vs]), vph, p)) break;
+                if (!wait_warp(c, B_(c.p_full[0]), pph0, p)) break;
                 pph0 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(0, vs, it.n > 1);
-                ptx::umma_commit(B_(c.o_full[0]));
-                if (!wait1(c, B_(c.p_full[1]), pph1, p)) break;
+                issue_pv(0, vs, n_tiles > 1);
+                commit(B_(c.o_full[0]));
+                if (!wait_warp(c, B_(c.p_full[1]), pph1, p)) break;
                 pph1 ^= 1;
                 ptx::tc_fence_after();
-                issue_pv(1, vs, it.n > 1);
-                ptx::umma_commit(B_(c.o_full[1]));
+                issue_pv(1, vs, n_tiles > 1);
+                commit(B_(c.o_full[1]));
             }
             // every MMA issued so far must finish before TMEM and shared memory go away
-            ptx::umma_commit(B_(c.teardown));
+            commit(B_(c.teardown));
             drain_bar(B_(c.teardown), 0, p.timeout_ns);
         }
         __syncwarp();
