@@ -16,7 +16,7 @@
 //   warp  8    scheduler + K producer (K_j into a 3-slot ring; K is consumed first, so it
 //              gets the deeper prefetch); it claims the next item early and pulls that
 //              item's Q into L2, and runs ahead into the next item's K tiles
-//   warp  9    TMEM allocator + single-thread MMA issuer
+//   warp  9    TMEM allocator + MMA issuer (warp-wide loop, one elected lane issues)
 //   warp 10    Q + V producer (the item's Q pair once the previous one is released, then
 //              V_j into a 2-slot ring)
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
