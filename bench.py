@@ -45,6 +45,15 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "sift_sparse_prefill_llama_32k.
 PROFILE_RAGGED = os.path.join(ROOT, "profiles", "sift_sparse_prefill_ragged_llama_32k_ragged.md")
 
 
+def profile_summary(workload: str) -> str:
+    """Committed ncu summary of the sparse kernel on `workload` (it may not exist)."""
+    if workload == "llama_32k":
+        return PROFILE_SUMMARY
+    if workload == "llama_32k_ragged":
+        return PROFILE_RAGGED
+    return os.path.join(ROOT, "profiles", f"sift_sparse_prefill_{workload}.md")
+
+
 def tile_flops(cfg) -> float:
     """FLOPs of one computed tile for one query head: QK^T and PV, 2*B*B*d each."""
     return 4.0 * cfg.tile * cfg.tile * cfg.head_dim
@@ -402,7 +411,7 @@ def run_ours(args, cfg):
 
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    traffic = None if shard else profiled_traffic(PROFILE_SUMMARY, cfg.name)
+    traffic = None if shard else profiled_traffic(profile_summary(cfg.name), cfg.name)
 
     # decode fused into the prefill: the same step without a separate decode
     fz0, fz1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -787,7 +796,7 @@ def run_ragged_line(args, cfg):
         "data": "synthetic", "config": config_dict(cfg, args, lay),
         "roofline": {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
                      "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak,
-                     "traffic": profiled_traffic(PROFILE_RAGGED, cfg.name),
+                     "traffic": profiled_traffic(profile_summary(cfg.name), cfg.name),
                      "kernel": "sift_sparse_prefill_ragged",
                      "peak_source": f"bf16_tflops_sustained of {peak_src}"},
         "gpu_launches": args.steps * r["gpu_launches_per_step"], "ragged": r,

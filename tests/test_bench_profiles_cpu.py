@@ -33,5 +33,5 @@ def test_traffic_null_without_a_summary(tmp_path):
 
 
 def test_committed_summaries_match_the_current_kernel():
-    assert bench.profiled_traffic(bench.PROFILE_SUMMARY, "llama_32k") is not None
-    assert bench.profiled_traffic(bench.PROFILE_RAGGED, "llama_32k_ragged") is not None
+    for workload in ("llama_32k", "llama_32k_ragged", "qwen3_64k", "llama_10doc", "batch4_p020"):
+        assert bench.profiled_traffic(bench.profile_summary(workload), workload) is not None, workload
