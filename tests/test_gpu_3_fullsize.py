@@ -99,3 +99,38 @@ def test_batch4_full_density_equals_dense(sift):
     assert (o.float() - od.float()).abs().max().item() <= 1e-2
     assert (lse - lsed).abs().max().item() <= 1e-4
     _check_layer(sift, cfg, lay, la, ca, 0, q, k, v, od, lsed, np.random.default_rng(5))
+
+
+def test_long_prompt_262k(sift):
+    """A maximum-size case: one prompt of 128 documents x 2,048 tokens + 256 (262,400
+    tokens, 2,050 query tiles, so rows of up to 2,050 key tiles), Llama-3.1-8B heads and
+    the 33K workload's bit statistics.  Decode is bit-exact; attention is checked on
+    sampled rows against the oracle and on every row against the convex bound."""
+    cfg = W.custom_config("long_262k", [([2048] * 128, 256)],
+                          W.BitSpec(head_density=(0.05, 0.35), head_ca_ratio=0.5),
+                          num_layers=1, num_q_heads=32, num_kv_heads=8, head_dim=128, tile=128)
+    lay, la, ca, prob, la_d, ca_d = setup(cfg)
+    st = prob.new_status()
+    ws = prob.new_workspace()
+    stream = torch.cuda.current_stream()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st, stream=stream)
+    kv_o, cnt_o = oracle.decode(lay, la, ca)
+    cnt_g = cnt.cpu().numpy()
+    assert np.array_equal(cnt_g, cnt_o)
+    kv_g = kv.cpu().numpy()
+    for h in (0, 7):
+        for i in (0, 1000, lay.num_tiles - 1):
+            n = int(cnt_o[0, h, i])
+            assert np.array_equal(kv_g[0, h, i, :n], kv_o[0, h, i, :n])
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    o, lse = sift.sparse_prefill(prob, 0, q, k, v, kv, cnt, sched, 0.0, None, None, ws, st,
+                                 stream)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, sift.status_string(int(st.item()))
+    rng = np.random.default_rng(17)
+    pairs = sample_pairs(lay, rng, n_random=3)
+    assert torch.isfinite(o.float()).all().item() and torch.isfinite(lse).all().item()
+    assert _convex_bound_ok(o, v, cfg.num_q_heads // cfg.num_kv_heads)
+    tok, head, O, LSE = oracle_rows_for_pairs(lay, la, ca, 0, q.cpu(), k.cpu(), v.cpu(), pairs)
+    og, lg = gpu_rows(o, lse, tok, head)
+    assert_attention_close(og, lg, O, LSE, "long 262K")
