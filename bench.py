@@ -91,6 +91,27 @@ def load_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def tensor_roofline(achieved: float, kernel: str, traffic, clocks=None) -> dict:
+    """Roofline entry of a tensor-bound kernel.  Each launch lasts about a millisecond and
+    the timed step tens of milliseconds, so the denominator is the burst bf16 rate (a
+    matmul timed on its own); the ratio to the sustained rate (seconds of back-to-back
+    matmuls under the power cap, at a lower clock) is kept beside it.  With the clocks
+    sampled during the timed region, `achieved_at_max_clock` scales the rate to the
+    maximum SM clock (rate / (median MHz / max MHz))."""
+    peaks, src = load_peaks()
+    burst = float(peaks.get("bf16_tflops"))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    r = {"bound": "tensor", "achieved": achieved, "peak": burst, "unit": "TFLOP/s",
+         "frac": achieved / burst, "traffic": traffic, "kernel": kernel,
+         "peak_source": f"bf16_tflops (burst) of {src}",
+         "peak_sustained": sustained, "frac_of_sustained": achieved / sustained}
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        scale = float(clocks["sm_mhz"]) / float(clocks["sm_max_mhz"])
+        r["achieved_at_max_clock"] = achieved / scale
+        r["frac_at_max_clock"] = achieved / scale / burst
+    return r
+
+
 def kernel_source_digest() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_vector_guided_gb300", "csrc")
@@ -409,8 +430,6 @@ def run_ours(args, cfg):
     kern_ms = float(layer_ms.mean())
     achieved = float(flops_layer.mean()) / (kern_ms * 1e-3) / 1e12
 
-    peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
     traffic = None if shard else profiled_traffic(profile_summary(cfg.name), cfg.name)
 
     # decode fused into the prefill: the same step without a separate decode
@@ -470,10 +489,6 @@ def run_ours(args, cfg):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(cfg, args, lay),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "sift_sparse_prefill",
-                     "peak_source": f"bf16_tflops_sustained of {peak_src}"},
         "gpu_launches": args.steps * (2 + L),
         "sparse_ms_per_layer": kern_ms,
         "sparse_ms_per_layer_p90": float(np.percentile(layer_ms.mean(axis=0), 90)),
@@ -496,6 +511,7 @@ def run_ours(args, cfg):
     }
     clocks = clk.summary()
     result["clocks"] = clocks
+    result["roofline"] = tensor_roofline(achieved, "sift_sparse_prefill", traffic, clocks)
 
     if not args.no_e2e:
         result["e2e"] = run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched,
@@ -723,8 +739,7 @@ def run_ragged(args, dev, stream, cfg=None, steps=3, warmup=2):
     d1.record(stream)
     torch.cuda.synchronize(dev)
     dense_ms = d0.elapsed_time(d1) / 3
-    peaks, _ = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    peak = float(load_peaks()[0].get("bf16_tflops"))
     ktf = float(fl.mean()) / (kern_ms * 1e-3) / 1e12
     return {"workload": cfg.name, "page": cfg.page, "query_tiles": NQ, "layers": L,
             "flops_per_step": float(fl.sum()),
@@ -753,6 +768,9 @@ def main(argv=None):
     ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
                     help="N > 1: every rank runs the whole workload (replicas, weak scaling) "
                          "or one range of kv heads of it (heads, strong scaling)")
+    ap.add_argument("--decode-only", action="store_true",
+                    help="profiling: time only sift_decode of the workload's bits (no Q/K/V "
+                         "on the device); prints its own JSON line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling only: keep the first N layers of the workload (the JSON "
                          "line then names the reduced workload)")
@@ -767,9 +785,56 @@ def main(argv=None):
                                   f" [first {args.layers} layers only]")
     if args.impl == "reference":
         return run_reference(args, cfg)
+    if args.decode_only:
+        return run_decode_only(args, cfg)
     if not W.make_layout(cfg).aligned:
         return run_ragged_line(args, cfg)
     return run_ours(args, cfg)
+
+
+def run_decode_only(args, cfg):
+    """sift_decode of every layer of the workload, alone: W warm-up and K timed calls,
+    CUDA events on the launching stream.  Only the bit words,
+    the lists, the counts and the schedule live on the device, so a profiler can capture
+    these launches at full size cheaply."""
+    import torch
+    import bit_vector_guided_gb300 as sift
+    from bit_vector_guided_gb300 import build as sbuild
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sbuild.build()
+    sift.load_library()
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    prob = sift.SiftProblem.from_layout(lay, dev)
+    la_d = torch.from_numpy(np.ascontiguousarray(la).view(np.int64)).to(dev)
+    ca_d = torch.from_numpy(np.ascontiguousarray(ca).view(np.int64)).to(dev)
+    L, H, N, R = cfg.num_layers, cfg.num_kv_heads, lay.num_tiles, lay.max_tiles_per_prompt
+    kv = torch.empty((L, H, N, R), dtype=torch.int32, device=dev)
+    cnt = torch.empty((L, H, N), dtype=torch.int32, device=dev)
+    sch = torch.empty((L, H * N), dtype=torch.int32, device=dev)
+    st = prob.new_status()
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        sift.decode(prob, la_d, ca_d, kv, cnt, sch, dev_status=st, stream=stream)
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    ev[0].record(stream)
+    for s_ in range(args.steps):
+        sift.decode(prob, la_d, ca_d, kv, cnt, sch, dev_status=st, stream=stream)
+        ev[s_ + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(st.item()) != 0:
+        raise RuntimeError("device status " + sift.status_string(int(st.item())))
+    us = [1e3 * ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    nbytes = decode_bytes(lay, cnt.cpu().numpy())
+    med = float(np.median(us))
+    print(json.dumps({"metric": "sift_decode us (all layers, one call)", "value": med,
+                      "unit": "us", "higher_is_better": False, "steps": args.steps,
+                      "warmup": args.warmup, "decode_bytes": nbytes,
+                      "decode_gbs": nbytes / (med * 1e-6) / 1e9,
+                      "config": config_dict(cfg, args, lay)}))
+    return 0
 
 
 def run_ragged_line(args, cfg):
@@ -787,20 +852,17 @@ def run_ragged_line(args, cfg):
     with ClockSampler(0) as clk:
         r = run_ragged(args, dev, stream, cfg=cfg, steps=args.steps, warmup=args.warmup)
     lay = W.make_layout(cfg)
-    peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    clocks = clk.summary()
     out = {
         "metric": METRIC, "value": r["tflops"], "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(cfg, args, lay),
-        "roofline": {"bound": "tensor", "achieved": r["kernel_tflops"], "peak": peak,
-                     "unit": "TFLOP/s", "frac": r["kernel_tflops"] / peak,
-                     "traffic": profiled_traffic(profile_summary(cfg.name), cfg.name),
-                     "kernel": "sift_sparse_prefill_ragged",
-                     "peak_source": f"bf16_tflops_sustained of {peak_src}"},
+        "roofline": tensor_roofline(r["kernel_tflops"], "sift_sparse_prefill_ragged",
+                                    profiled_traffic(profile_summary(cfg.name), cfg.name),
+                                    clocks),
         "gpu_launches": args.steps * r["gpu_launches_per_step"], "ragged": r,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     print(json.dumps(out))
     return 0

@@ -75,13 +75,18 @@ int64_t max_query_tiles(const sift_problem *p) {
 }
 
 int device_sm_count() {
-    static int cache[64] = {0};
+    // several host threads may launch at once: each slot is read and written atomically
+    // (a race only repeats the attribute query, which returns the same value)
+    static std::atomic<int> cache[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-    if (dev < 64 && cache[dev] > 0) return cache[dev];
+    if (dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev < 64) cache[dev] = n;
+    if (dev < 64) cache[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 

@@ -10,9 +10,14 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its kNoAllocScratchBytes until the process exits.  Host code
-// cannot use the symbol as a device address, so the first call on each device
-// asks the runtime for the array's address (cudaGetSymbolAddress, with that
-// device current) and caches it.
+// cannot use the symbol as a device address, so a call asks the runtime for
+// the array's address (cudaGetSymbolAddress, with the device current) and
+// caches it together with the unique id of the context it was taken in.  A
+// later call from another context of that device -- after cudaDeviceReset
+// destroyed the primary context and a new one took its place, for instance --
+// sees a different id and looks the address up again.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "sift_internal.h"
@@ -25,21 +30,57 @@ constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {nullptr};
+struct ScratchSlot {
+    unsigned long long ctx_id;  // context the address was taken in (0: none yet)
+    void *ptr;
+};
 
-// address of this device's copy of the array; nullptr on failure
+std::mutex g_setup_mutex;
+ScratchSlot g_slot[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// unique id (for the life of the process) of the calling thread's current context;
+// false when there is none or it cannot be read
+bool current_context_id(unsigned long long *id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *a = nullptr, *b = nullptr;
+        cudaDriverEntryPointQueryResult qa, qb;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault,
+                                             &qa) == cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+            get_id = reinterpret_cast<CtxGetIdFn>(b);
+        }
+    });
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// address of this device's copy of the array in the current context; nullptr on failure
 void *scratch_for_current_device() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
-            return nullptr;
-        g_scratch_ptr[dev] = ptr;
-    }
-    return g_scratch_ptr[dev];
+    unsigned long long id = 0;
+    if (current_context_id(&id) && g_slot[dev].ctx_id == id && g_slot[dev].ptr != nullptr)
+        return g_slot[dev].ptr;
+    // first call in this context (the lookup also makes the device's context current)
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+        return nullptr;
+    if (!current_context_id(&id)) id = 0;  // unknown context: look it up again next time
+    g_slot[dev] = ScratchSlot{id, ptr};
+    return ptr;
 }
 
 }  // namespace

@@ -203,6 +203,10 @@ sift_status sift_dense_prefill(const sift_problem *prob, const void *q, const vo
  *     units) is rejected with SIFT_ERR_UNSUPPORTED before anything is enqueued.
  *   - The first call on a device looks up the array's device address, with
  *     that device current; make that first call outside any stream capture.
+ *     The address is kept with the id of the context it was taken in.  A
+ *     call from another context of the device (after cudaDeviceReset
+ *     replaced the primary context, for instance) looks it up again, so the
+ *     first call after such a reset must also be made outside stream capture.
  *   - Every call shares the one array and it keeps the last call's contents:
  *     calls whose work may overlap on the GPU (different streams, or several
  *     host threads) race on it and must be serialised by the caller.

@@ -58,10 +58,10 @@ def assert_attention_close(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     return mx, mean, lrel
 
 
-def sample_pairs(lay, rng, n_random=24):
+def sample_pairs(lay, rng, n_random=64):
     """(query tile, query head) pairs to check on a large batch: the first tile of each
-    prompt, the last document tile and the last suffix tile of each prompt, plus random
-    ones."""
+    prompt, the last document tile and the last suffix tile of each prompt, plus
+    n_random distinct random ones (so at least n_random pairs in all)."""
     B = lay.tile
     Hq = lay.num_q_heads
     pairs = set()
@@ -73,9 +73,21 @@ def sample_pairs(lay, rng, n_random=24):
         for t in (t0, last_doc_tile, t1 - 1):
             pairs.add((t, int(rng.integers(Hq))))
     N = lay.num_tiles
-    for _ in range(n_random):
+    target = len(pairs) + min(n_random, N * Hq - len(pairs))
+    while len(pairs) < target:
         pairs.add((int(rng.integers(N)), int(rng.integers(Hq))))
     return sorted(pairs)
+
+
+def compare_decode(lay, kv_gpu, cnt_gpu, kv_o, cnt_o):
+    """Decoded lists bit-exact against the oracle's: every count, and every entry up to
+    each row's count (entries past it are not written by the kernel)."""
+    cnt_g = cnt_gpu.cpu().numpy() if hasattr(cnt_gpu, "cpu") else np.asarray(cnt_gpu)
+    kv_g = kv_gpu.cpu().numpy() if hasattr(kv_gpu, "cpu") else np.asarray(kv_gpu)
+    assert np.array_equal(cnt_g, cnt_o), "counts differ from the oracle"
+    R = kv_o.shape[-1]
+    mask = np.arange(R, dtype=np.int32)[None, None, None, :] < cnt_o[..., None]
+    assert np.array_equal(np.where(mask, kv_g, -1), kv_o), "lists differ from the oracle"
 
 
 def oracle_rows_for_pairs(lay, la, ca, layer, q, k, v, pairs):

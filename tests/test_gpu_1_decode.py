@@ -89,7 +89,8 @@ def test_decode_edge_cases(sift, cfg):
 
 
 @pytest.mark.parametrize("name", ["tiny", "llama_10doc", "llama_32k", "qwen3_64k", "batch4_p005",
-                                  "batch4_p020", "batch4_p100"])
+                                  "batch4_p010", "batch4_p020", "batch4_p040", "batch4_p070",
+                                  "batch4_p100"])
 def test_decode_benchmark_configs(sift, name):
     lay, la, ca, prob, la_d, ca_d = setup(W.get_config(name))
     st = prob.new_status()

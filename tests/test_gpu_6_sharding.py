@@ -1,12 +1,15 @@
 """KV-head shards run through the unchanged C ABI reproduce the head slices of the
-unsharded prefill bitwise (each work item reads only its own kv head)."""
+unsharded prefill bitwise (each work item reads only its own kv head), and each
+shard's decode and attention agree with the oracle run on the unsharded layout,
+restricted to the shard's heads (bit-exact lists, outputs within the tolerance)."""
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from bit_vector_guided_gb300.sharding import kv_head_range, shard_bits
-from helpers import device_bits, setup
+from helpers import assert_attention_close, device_bits, setup
 
 pytestmark = pytest.mark.gpu
 
@@ -29,9 +32,11 @@ def test_shards_match_unsharded(sift, world):
     G = cfg.num_q_heads // cfg.num_kv_heads
     st = prob.new_status()
     kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st)
+    kv_o, cnt_o = oracle.decode(lay, la, ca)
     for layer in range(cfg.num_layers):
         q, k, v = W.make_qkv(cfg, layer, device="cuda")
         o, lse = sift.sparse_prefill(prob, layer, q, k, v, kv, cnt, sched, dev_status=st)
+        O_ref, LSE_ref = oracle.attention_all(lay, la, ca, layer, q.cpu(), k.cpu(), v.cpu())
         for r in range(world):
             h0, h1 = kv_head_range(r, world, cfg.num_kv_heads)
             la_off, ca_off, la_s, ca_s = shard_bits(lay.cu_seqlens, lay.doc_cu, lay.doc_end,
@@ -57,6 +62,14 @@ def test_shards_match_unsharded(sift, world):
             assert torch.equal(cnt_s, cnt[:, h0:h1])
             assert torch.equal(o_s, o[:, h0 * G:h1 * G]) and torch.equal(o_f, o_s)
             assert torch.equal(lse_s, lse[h0 * G:h1 * G]) and torch.equal(lse_f, lse_s)
+            # the shard against the oracle of the whole problem, restricted to its heads
+            kv_sh, cnt_sh = kv_s.cpu().numpy(), cnt_s.cpu().numpy()
+            assert np.array_equal(cnt_sh, cnt_o[:, h0:h1])
+            m = np.arange(kv_o.shape[-1])[None, None, None, :] < cnt_o[:, h0:h1, :, None]
+            assert np.array_equal(np.where(m, kv_sh, -1), kv_o[:, h0:h1])
+            assert_attention_close(o_s.double().cpu().numpy(), lse_s.double().cpu().numpy(),
+                                   O_ref[:, h0 * G:h1 * G], LSE_ref[h0 * G:h1 * G],
+                                   f"shard {r}/{world} layer {layer}")
         assert int(st.item()) == 0
 
 
@@ -76,6 +89,7 @@ def test_general_layout_shards_match_unsharded(sift, world):
     q, k, v = W.make_qkv(cfg, 0, device="cuda")
     o, lse = sift.sparse_prefill_ragged(prob, 0, q, k, v, *lists, dev_status=st)
     G = cfg.num_q_heads // cfg.num_kv_heads
+    O_ref, LSE_ref = oracle.attention_all(lay, la, ca, 0, q.cpu(), k.cpu(), v.cpu())
     for r in range(world):
         h0, h1 = kv_head_range(r, world, cfg.num_kv_heads)
         la_off, ca_off, la_s, ca_s = shard_bits(lay.cu_seqlens, lay.doc_cu, lay.doc_end,
@@ -97,4 +111,7 @@ def test_general_layout_shards_match_unsharded(sift, world):
         assert int(ss.item()) == 0
         assert torch.equal(o_s, o[:, h0 * G:h1 * G])
         assert torch.equal(lse_s, lse[h0 * G:h1 * G])
+        assert_attention_close(o_s.double().cpu().numpy(), lse_s.double().cpu().numpy(),
+                               O_ref[:, h0 * G:h1 * G], LSE_ref[h0 * G:h1 * G],
+                               f"general-layout shard {r}/{world}")
     assert int(st.item()) == 0
