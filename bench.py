@@ -73,6 +73,18 @@ def decode_bytes(lay, counts: np.ndarray) -> float:
                  4 * units + 4 * units + 4 * units)
 
 
+def decode_launches(lay) -> int:
+    """Kernel launches of one sift_decode call (the library's rule): one while the
+    schedule blocks' shared memory -- (rowcap + 1 + Hkv*D + 2*D + N) x 4 bytes, plus
+    Hkv*N x 4 for the counts when the total stays within 226 KB -- fits in 32 KB, else
+    two."""
+    base = 4 * (lay.max_tiles_per_prompt + 1 + lay.num_kv_heads * lay.num_docs +
+                2 * lay.num_docs + lay.num_tiles)
+    cnt = 4 * lay.num_kv_heads * lay.num_tiles
+    need = base + (cnt if base + cnt <= 226 * 1024 else 0)
+    return 1 if need <= 32 * 1024 else 2
+
+
 def useful_fraction(cfg, lay, flops_step: float) -> float:
     """Share of the computed-tile FLOPs that are not masked out on the diagonal: every row
     holds one diagonal tile, of which (B+1)/(2B) is causal."""
@@ -489,7 +501,7 @@ def run_ours(args, cfg):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
         "scaling": "strong" if shard else "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config_dict(cfg, args, lay),
-        "gpu_launches": args.steps * (2 + L),
+        "gpu_launches": args.steps * (decode_launches(lay) + L),
         "sparse_ms_per_layer": kern_ms,
         "sparse_ms_per_layer_p90": float(np.percentile(layer_ms.mean(axis=0), 90)),
         "dense_ms_per_layer": dense_ms_layer,
@@ -506,7 +518,7 @@ def run_ours(args, cfg):
         "fused_ms_per_step": fused_ms_step,
         "fused_ms_per_layer": fused_ms_step / L,
         "fused_tflops": flops_step / (fused_ms_step * 1e-3) / 1e12,
-        "decode_launches_per_step": 2,
+        "decode_launches_per_step": decode_launches(lay),
         "build_bits_ms_per_layer": build_ms_layer,
     }
     clocks = clk.summary()
@@ -611,12 +623,39 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
         step()
     torch.cuda.synchronize(dev)
     el = max_over_ranks(time.perf_counter() - t0, dist, dev)
+
+    # The host link's own floor for these bytes: the same copies on the same two streams
+    # (uploads on one, read-backs on the other, running at once), with no kernels.
+    def copies_only():
+        with torch.cuda.stream(up):
+            la_d.copy_(la_h, non_blocking=True)
+            ca_d.copy_(ca_h, non_blocking=True)
+            for l in range(L):
+                for dst, src in zip(qkv[l], host_in[l]):
+                    dst.copy_(src, non_blocking=True)
+        with torch.cuda.stream(down):
+            for l in range(L):
+                host_out[l][0].copy_(outs[l][0], non_blocking=True)
+                host_out[l][1].copy_(outs[l][1], non_blocking=True)
+
+    copies_only()
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    for _ in range(steps):
+        copies_only()
+    torch.cuda.synchronize(dev)
+    floor = max_over_ranks(time.perf_counter() - t1, dist, dev) / steps
     return {"value": whole_job_tflops(job_flops_step, steps, el, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "ms_per_step": 1e3 * el / steps, "steps": steps,
+            "link_floor_ms_per_step": 1e3 * floor,
+            "link_gbs": (h2d + d2h) / floor / 1e9,
+            "ratio_to_link_floor": (el / steps) / floor,
             "note": "pinned host buffers; H2D of each layer's Q/K/V on one copy stream and "
                     "D2H of its O/LSE on another, both overlapping the kernels; consecutive "
-                    "steps pipeline (each buffer waits only for its own last use)"}
+                    "steps pipeline (each buffer waits only for its own last use). "
+                    "link_floor_ms_per_step: the same copies alone on the same streams, "
+                    "both directions at once, no kernels"}
 
 
 def run_sweep(args, dev, stream):
@@ -819,6 +858,9 @@ def run_decode_only(args, cfg):
         sift.decode(prob, la_d, ca_d, kv, cnt, sch, dev_status=st, stream=stream)
     torch.cuda.synchronize(dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    # keep the GPU busy while the host queues every timed call, so that the events measure
+    # the device and not the host's launch rate
+    torch.cuda._sleep(int(2e7))
     ev[0].record(stream)
     for s_ in range(args.steps):
         sift.decode(prob, la_d, ca_d, kv, cnt, sch, dev_status=st, stream=stream)

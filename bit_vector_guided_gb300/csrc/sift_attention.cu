@@ -1178,6 +1178,7 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
                                            void *workspace, size_t workspace_bytes,
                                            int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_sparse_prefill");
     if (prob == nullptr || layer < 0 || layer >= prob->num_layers || kv_idx == nullptr ||
         counts == nullptr || sched == nullptr)
         return SIFT_ERR_INVALID_ARG;
@@ -1204,6 +1205,7 @@ extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int3
                                                   size_t workspace_bytes, int32_t *dev_status,
                                                   cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_sparse_prefill_ragged");
     if (prob == nullptr || layer < 0 || layer >= prob->num_layers || qtiles == nullptr ||
         kv == nullptr || counts == nullptr || sched == nullptr || num_query_tiles < 1 ||
         (reinterpret_cast<uintptr_t>(kv) & 7u) != 0)
@@ -1255,6 +1257,7 @@ extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_dense_prefill");
     CUtensorMap maps[5];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
@@ -1281,6 +1284,7 @@ extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t laye
                                           void *workspace, size_t workspace_bytes,
                                           int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_fused_prefill");
     if (prob == nullptr || layer < 0 || layer >= prob->num_layers) return SIFT_ERR_INVALID_ARG;
     if ((prob->la_words_len > 0 && la_words == nullptr) ||
         (prob->ca_words_len > 0 && ca_words == nullptr))

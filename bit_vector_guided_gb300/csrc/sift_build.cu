@@ -326,6 +326,7 @@ extern "C" sift_status sift_build_bits(const sift_problem *prob, int32_t layer, 
                                        size_t workspace_bytes, int32_t *dev_status,
                                        cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_build_bits");
     sift_status st = validate_any(prob);
     if (st != SIFT_OK) return st;
     if (layer < 0 || layer >= prob->num_layers || q == nullptr || k == nullptr ||

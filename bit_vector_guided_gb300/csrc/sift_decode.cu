@@ -2,21 +2,24 @@
 // a custom kernel turns the LA/CA bit vectors into explicit tile indices) and
 // the longest-first schedule consumed by the persistent attention kernel.
 //
-// One warp decodes all rows of one (layer, kv head, document) -- or of one prompt's
-// query suffix.  Candidate tiles arrive as 64-bit words (the CA words of every earlier
-// document of the prompt, then each row's own LA word(s)); every lane sees the same
-// word, tests its own bit, and takes its output slot from the popcount of the lower
-// lanes' bits, so each 32-bit half-word is compacted with one popc and written with
-// one coalesced store.  The CA prefix is the same for every row of a document, so it
-// is compacted once per document and copied; document metadata for up to 32 earlier
-// documents, and the first LA word of up to 32 rows, are fetched by the 32 lanes at
-// once and broadcast with shuffles.
+// One launch does both.  Its first L blocks are the schedule of the L layers:
+// block l counts every row of layer l straight from the bits (the CA pages of the
+// earlier documents, popcounts over each document once; the row's LA tiles; the
+// diagonal; dense rows in the suffix), then sorts the rows longest-first with a
+// counting sort in shared memory.  The other blocks write the lists, one block of
+// four warps per (layer, kv head, document or suffix): the CA prefix -- the same
+// for every row of a document -- is compacted once, by a block-wide scan over the
+// earlier documents' popcounts, then each warp takes every fourth row: the
+// prefix, its own LA tiles (each lane tests one bit; the slot is the popcount of
+// the lower lanes' bits) and the diagonal.  Both halves read only the bits, so
+// they run side by side.
+#include <climits>
+
 #include "ptx.cuh"
 #include "sift_internal.h"
 
 namespace sift {
 namespace {
-
 
 struct DecodeArgs {
     const int32_t *cu;
@@ -29,10 +32,16 @@ struct DecodeArgs {
     int64_t la_len, ca_len;
     int32_t *kv_idx;
     int32_t *counts;
+    int32_t *sched;
     int32_t *status;
-    int P, D, Hkv, B, N, rowcap;
-    int64_t rows;
+    int P, D, L, Hkv, B, N, rowcap;
+    int sched_blocks;    // blocks [0, sched_blocks) count and schedule one layer each
+    int64_t seg_blocks;  // then one block per (layer, kv head, segment)
+    int cnt_smem;        // the schedule blocks keep the layer's counts in shared memory
 };
+
+constexpr int kDecThreads = 256;
+constexpr int kPrefixCap = 2048;  // CA prefix entries staged in shared memory
 
 __device__ __forceinline__ void set_status(int32_t *st, int code) {
     if (st) atomicCAS(st, 0, code);
@@ -45,6 +54,67 @@ __device__ __forceinline__ int find_prompt(const int32_t *cu, int P, int64_t tok
         if (__ldg(cu + mid) <= tok) lo = mid; else hi = mid - 1;
     }
     return lo;
+}
+
+// the prompt owning document g: the last p with doc_cu[p] <= g
+__device__ __forceinline__ int doc_prompt(const int32_t *doc_cu, int P, int g) {
+    int lo = 0, hi = P - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(doc_cu + mid) <= g) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ uint64_t low_bits(uint64_t word, int nb) {
+    return nb >= 64 ? word : (nb <= 0 ? 0ull : (word & ((1ull << nb) - 1ull)));
+}
+
+// Document g of prompt p: first token ds and tile count T; false when its bounds are
+// inconsistent (not multiples of B, empty, outside the prompt)
+__device__ __forceinline__ bool doc_span(const DecodeArgs &a, int p, int g, int &ds, int &T) {
+    const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
+    const int g0 = __ldg(a.doc_cu + p);
+    ds = (g == g0) ? p0 : __ldg(a.doc_end + g - 1);
+    const int de = __ldg(a.doc_end + g);
+    T = 0;
+    if (p0 % a.B || ds % a.B || de % a.B || de <= ds || ds < p0 || de > p1) return false;
+    T = (de - ds) / a.B;
+    return true;
+}
+
+// number of set bits among the T CA bits of document g for (layer, kv head); -1 when the
+// words lie outside the array
+__device__ __forceinline__ int ca_popcount(const DecodeArgs &a, int g, int T, int64_t lh) {
+    const int W = (T + 63) / 64;
+    const int64_t off = __ldg(a.ca_off + g) + lh * W;
+    if (off < 0 || off + W > a.ca_len) return -1;
+    int n = 0;
+    for (int wi = 0; wi < W; ++wi) n += __popcll(low_bits(__ldg(a.ca + off + wi), T - 64 * wi));
+    return n;
+}
+
+// exclusive prefix sum over the block; *total receives the sum
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_sums[wid] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < kDecThreads / 32; ++w) {
+        const int ws = warp_sums[w];
+        if (w < wid) before += ws;
+        all += ws;
+    }
+    __syncthreads();  // warp_sums may be reused by the next scan
+    *total = all;
+    return before + incl - v;
 }
 
 struct RowWriter {
@@ -70,30 +140,166 @@ struct RowWriter {
     }
 };
 
-// One warp per segment of a (layer, kv head): a document of a prompt, or a prompt's
-// query suffix.  Every row of a document shares the same CA prefix (the flagged pages
-// of the earlier documents), so the warp compacts that prefix once -- into shared
-// memory and into the document's first row -- and then writes each row as prefix +
-// its own LA tiles + the diagonal.  Suffix rows list every tile of the prompt up to
-// the diagonal.
-constexpr int kSegWarps = 4;
-constexpr int kPrefixCap = 1024;  // CA prefix entries staged in shared memory per warp
+// ---- schedule blocks: every row count of layer l from the bits, then the counting sort
+// Shared memory: hist[rowcap + 1] | cap[Hkv * D] (CA prefix count of (kv head, document))
+// | dstart[D], dT[D] (first tile and tile count of each document, dT = -1 when bad)
+// | tinfo[N] (tile i: its document g >= 0, or -1 - p for the suffix of prompt p)
+// | cnts[Hkv * N] (the counts again, when a.cnt_smem; else they are read back)
+constexpr int kTileUnset = INT_MIN;
 
-__global__ void __launch_bounds__(kSegWarps * 32)
-decode_segments_kernel(const DecodeArgs a) {
-    __shared__ int32_t prefix_smem[kSegWarps][kPrefixCap];
+__device__ void schedule_layer(const DecodeArgs &a, int l, int32_t *smem) {
+    __shared__ int warp_sums[kDecThreads / 32];
+    const int tid = threadIdx.x;
+    const int nb = a.rowcap + 1;
+    const int U = a.Hkv * a.N;
+    int *hist = smem;
+    int *cap = hist + nb;
+    int *dstart = cap + a.Hkv * a.D;
+    int *dT = dstart + a.D;
+    int *tinfo = dT + a.D;
+    int *cnts = tinfo + a.N;
+    for (int b = tid; b < nb; b += kDecThreads) hist[b] = 0;
+    for (int i = tid; i < a.N; i += kDecThreads) tinfo[i] = kTileUnset;
+    __syncthreads();
+    for (int g = tid; g < a.D; g += kDecThreads) {
+        const int p = doc_prompt(a.doc_cu, a.P, g);
+        int ds = 0, T = 0;
+        const bool ok = doc_span(a, p, g, ds, T);
+        if (!ok) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+        dstart[g] = ds / a.B;
+        dT[g] = ok ? T : -1;
+        for (int r = 0; r < T; ++r) tinfo[ds / a.B + r] = g;
+    }
+    for (int p = tid; p < a.P; p += kDecThreads) {
+        const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
+        const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
+        int sstart = p0;
+        if (g0 >= 0 && g0 < g1 && g1 <= a.D) sstart = __ldg(a.doc_end + g1 - 1);
+        if (p0 % a.B || p1 % a.B || sstart % a.B || sstart < p0 || sstart > p1 || p1 > a.N * a.B) {
+            set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+            continue;
+        }
+        for (int i = sstart / a.B; i < p1 / a.B; ++i) tinfo[i] = -1 - p;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < a.Hkv * a.D; idx += kDecThreads) {
+        const int h = idx / a.D, g = idx - (idx / a.D) * a.D;
+        int n = 0;
+        if (dT[g] > 0) {
+            n = ca_popcount(a, g, dT[g], static_cast<int64_t>(l) * a.Hkv + h);
+            if (n < 0) {
+                set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+                n = 0;
+            }
+        }
+        cap[idx] = n;
+    }
+    __syncthreads();
+    // CA prefix of each document: the flagged pages of the earlier documents of its prompt
+    for (int idx = tid; idx < a.Hkv * a.P; idx += kDecThreads) {
+        const int h = idx / a.P, p = idx - (idx / a.P) * a.P;
+        const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
+        int run = 0;
+        for (int g = max(g0, 0); g < min(g1, a.D); ++g) {
+            const int c = cap[h * a.D + g];
+            cap[h * a.D + g] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    // every row: prefix + LA tiles below the diagonal + the diagonal; suffix rows dense.
+    // Four rows per thread and round, their first LA words loaded before any is used.
+    int32_t *cnt = a.counts + static_cast<int64_t>(l) * U;
+    constexpr int kR = 4;
+    for (int u0 = tid; u0 < U; u0 += kR * kDecThreads) {
+        int n[kR];
+        uint64_t w0[kR];
+        int64_t row[kR];
+        int il[kR], W[kR];
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+            const int u = u0 + k * kDecThreads;
+            n[k] = 0;
+            w0[k] = 0;
+            row[k] = -1;
+            il[k] = 0;
+            W[k] = 1;
+            if (u >= U) continue;
+            const int h = u / a.N, i = u - (u / a.N) * a.N;
+            const int info = tinfo[i];
+            if (info >= 0 && dT[info] > 0) {
+                const int g = info, T = dT[g];
+                W[k] = (T + 63) / 64;
+                il[k] = i - dstart[g];
+                const int64_t r = __ldg(a.la_off + g) +
+                                  ((static_cast<int64_t>(l) * a.Hkv + h) * T + il[k]) * W[k];
+                n[k] = cap[h * a.D + g] + 1;
+                if (r < 0 || r + W[k] > a.la_len) {
+                    set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+                } else {
+                    row[k] = r;
+                    if (il[k] > 0) w0[k] = __ldg(a.la + r);
+                }
+            } else if (info != kTileUnset && info < 0) {
+                n[k] = i - __ldg(a.cu + (-1 - info)) / a.B + 1;  // the query suffix: dense
+            } else {
+                set_status(a.status, SIFT_ERR_DEVICE_CHECK);  // a tile of no segment
+                n[k] = 1;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kR; ++k) {
+            const int u = u0 + k * kDecThreads;
+            if (u >= U) continue;
+            if (row[k] >= 0 && il[k] > 0) {
+                n[k] += __popcll(low_bits(w0[k], il[k]));
+                for (int wi = 1; 64 * wi < il[k]; ++wi)
+                    n[k] += __popcll(low_bits(__ldg(a.la + row[k] + wi), il[k] - 64 * wi));
+            }
+            int v = n[k];
+            if (v > a.rowcap || v < 1) {
+                set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+                v = v < 1 ? 1 : a.rowcap;
+            }
+            cnt[u] = v;
+            if (a.cnt_smem) cnts[u] = v;
+            atomicAdd(&hist[v], 1);
+        }
+    }
+    __syncthreads();
+    // exclusive scan over the bins in descending count order (bin rowcap first)
+    const int per = (nb + kDecThreads - 1) / kDecThreads;
+    const int r0 = tid * per, r1 = min(r0 + per, nb);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) local += hist[a.rowcap - r];
+    int total = 0;
+    int run = block_exclusive_scan(local, warp_sums, &total);
+    for (int r = r0; r < r1; ++r) {
+        const int b = a.rowcap - r;
+        const int v = hist[b];
+        hist[b] = run;
+        run += v;
+    }
+    __syncthreads();
+    int32_t *sch = a.sched + static_cast<int64_t>(l) * U;
+    for (int u = tid; u < U; u += kDecThreads) {
+        const int c = a.cnt_smem ? cnts[u] : cnt[u];
+        const int pos = atomicAdd(&hist[c], 1);
+        if (pos < U) sch[pos] = u;
+    }
+}
+
+// ---- list blocks: all rows of one (layer, kv head, document) or one prompt's suffix
+__device__ void decode_segment(const DecodeArgs &a, int64_t w, int32_t *pre) {
+    __shared__ int warp_sums[kDecThreads / 32];
+    const int tid = threadIdx.x;
     const uint32_t lane = threadIdx.x & 31u;
-    const int wib = static_cast<int>(threadIdx.x >> 5);
-    const int64_t w = static_cast<int64_t>(blockIdx.x) * kSegWarps + wib;
+    const int wid = threadIdx.x >> 5;
     const int S = a.D + a.P;
-    if (w >= a.rows) return;  // rows = layers * Hkv * segments here
     const int seg = static_cast<int>(w % S);
     const int64_t lh = w / S;  // layer * Hkv + kv head
-    const int h = static_cast<int>(lh % a.Hkv);
-    const int l = static_cast<int>(lh / a.Hkv);
     const int B = a.B;
     const int64_t rowbase = lh * a.N;  // row of global tile 0 for this (layer, kv head)
-    int32_t *pre = prefix_smem[wib];
 
     if (seg >= a.D) {
         // ---- the query suffix of prompt p: dense over the prompt
@@ -101,137 +307,103 @@ decode_segments_kernel(const DecodeArgs a) {
         const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
         const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
         if (p0 % B || p1 % B || p0 > p1 || g0 < 0 || g0 > g1 || g1 > a.D) {
-            if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+            if (tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
             return;
         }
         const int sstart = g1 > g0 ? __ldg(a.doc_end + g1 - 1) : p0;
         if (sstart % B || sstart < p0 || sstart > p1) {
-            if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+            if (tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
             return;
         }
         const int pt = p0 / B;
-        for (int i = sstart / B; i < p1 / B; ++i) {
+        for (int i = sstart / B + wid; i < p1 / B; i += kDecThreads / 32) {
             int32_t *out = a.kv_idx + (rowbase + i) * a.rowcap;
-            int n = i - pt + 1;
-            if (n > a.rowcap) {
-                if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
-                n = a.rowcap;
-            }
+            const int n = min(i - pt + 1, a.rowcap);  // a longer row is reported by the counts
             for (int k = static_cast<int>(lane); k < n; k += 32) out[k] = pt + k;
-            if (lane == 0) a.counts[rowbase + i] = n;
         }
         return;
     }
 
     // ---- document g
     const int g = seg;
-    int lo = 0, hi = a.P - 1;  // prompt owning g: the last p with doc_cu[p] <= g
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(a.doc_cu + mid) <= g) lo = mid; else hi = mid - 1;
-    }
-    const int p = lo;
-    const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
+    const int p = doc_prompt(a.doc_cu, a.P, g);
+    const int p0 = __ldg(a.cu + p);
     const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
-    const int ds = (g == g0) ? p0 : __ldg(a.doc_end + g - 1);
-    const int de = __ldg(a.doc_end + g);
-    if (g < g0 || g >= g1 || p0 % B || ds % B || de % B || de <= ds || ds < p0 || de > p1) {
-        if (lane == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+    int ds = 0, T = 0;
+    if (g < g0 || g >= g1 || !doc_span(a, p, g, ds, T)) {
+        if (tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
         return;
     }
-    const int T = (de - ds) / B;
     const int W = (T + 63) / 64;
     const int t0 = ds / B;
-    int32_t *row0 = a.kv_idx + (rowbase + t0) * a.rowcap;
-    bool bad = false;
+    int32_t *rows = a.kv_idx + (rowbase + t0) * a.rowcap;  // row il at rows + il*rowcap
 
-    // CA prefix of the earlier documents, 32 documents per round trip
-    int c = 0;  // warp-uniform
-    for (int base = g0; base < g; base += 32) {
-        const int gk = base + static_cast<int>(lane);
-        int dsk = 0, Tk = 0;
+    // CA prefix of the earlier documents, 128 documents per round: each thread counts one
+    // document's flagged pages, a block scan places them, each thread writes its pages
+    int c = 0;  // block-uniform
+    for (int base = g0; base < g; base += kDecThreads) {
+        const int gk = base + tid;
+        int dsk = 0, Tk = 0, cnt = 0;
         int64_t offk = 0;
-        uint64_t w0 = 0;
         if (gk < g) {
-            dsk = (gk == g0) ? p0 : __ldg(a.doc_end + gk - 1);
-            const int dek = __ldg(a.doc_end + gk);
-            Tk = (dek - dsk) / B;
-            const int Wk = (Tk + 63) / 64;
-            offk = __ldg(a.ca_off + gk) + (static_cast<int64_t>(l) * a.Hkv + h) * Wk;
-            if (dek <= dsk || (dek - dsk) % B != 0 || dsk % B != 0 || offk < 0 ||
-                offk + Wk > a.ca_len) {
-                bad = true;
+            if (!doc_span(a, p, gk, dsk, Tk)) {
+                set_status(a.status, SIFT_ERR_DEVICE_CHECK);
                 Tk = 0;
             } else {
-                w0 = __ldg(a.ca + offk);
-            }
-        }
-        const int nd = min(32, g - base);
-        for (int k = 0; k < nd; ++k) {
-            const int Tq = __shfl_sync(0xffffffffu, Tk, k);
-            const int dsq = __shfl_sync(0xffffffffu, dsk, k);
-            const int64_t offq = __shfl_sync(0xffffffffu, offk, k);
-            const uint64_t wq = __shfl_sync(0xffffffffu, w0, k);
-            const int Wq = (Tq + 63) / 64;
-            for (int wi = 0; wi < Wq; ++wi) {
-                const uint64_t word = wi == 0 ? wq : __ldg(a.ca + offq + wi);
-                const int nb = min(64, Tq - 64 * wi);
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    const int rem = nb - 32 * half;
-                    if (rem <= 0) break;
-                    uint32_t bits = static_cast<uint32_t>(word >> (32 * half));
-                    if (rem < 32) bits &= (1u << rem) - 1u;
-                    if (bits == 0) continue;
-                    if ((bits >> lane) & 1u) {
-                        const int pos = c + __popc(bits & ((1u << lane) - 1u));
-                        const int tile = dsq / B + 64 * wi + 32 * half + static_cast<int>(lane);
-                        if (pos < kPrefixCap) pre[pos] = tile;
-                        if (pos < a.rowcap) row0[pos] = tile;
-                    }
-                    c += __popc(bits);
+                const int Wk = (Tk + 63) / 64;
+                offk = __ldg(a.ca_off + gk) + lh * Wk;
+                if (offk < 0 || offk + Wk > a.ca_len) {
+                    set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+                    Tk = 0;
+                } else {
+                    for (int wi = 0; wi < Wk; ++wi)
+                        cnt += __popcll(low_bits(__ldg(a.ca + offk + wi), Tk - 64 * wi));
                 }
             }
         }
+        int total = 0;
+        int pos = c + block_exclusive_scan(cnt, warp_sums, &total);
+        for (int wi = 0; 64 * wi < Tk; ++wi) {
+            uint64_t word = low_bits(__ldg(a.ca + offk + wi), Tk - 64 * wi);
+            while (word) {
+                const int b = __ffsll(static_cast<long long>(word)) - 1;
+                word &= word - 1;
+                const int tile = dsk / B + 64 * wi + b;
+                if (pos < kPrefixCap) {
+                    pre[pos] = tile;
+                } else if (pos < a.rowcap) {  // rare: beyond the staged prefix, straight to every row
+                    for (int r = 0; r < T; ++r) rows[static_cast<int64_t>(r) * a.rowcap + pos] = tile;
+                }
+                ++pos;
+            }
+        }
+        c += total;
     }
-    __syncwarp();
+    __syncthreads();
 
-    // rows of the document: prefix, LA tiles j < il, diagonal
-    const int64_t la_base = __ldg(a.la_off + g) + (static_cast<int64_t>(l) * a.Hkv + h) * T * W;
-    if (la_base < 0 || la_base + static_cast<int64_t>(T) * W > a.la_len) bad = true;
-    bad = __any_sync(0xffffffffu, bad);  // warp-uniform from here on
-    const int cc = min(c, a.rowcap);
-    for (int rb = 0; rb < T; rb += 32) {
-        // first LA word of 32 rows in one round trip
-        const int rl = rb + static_cast<int>(lane);
-        uint64_t lw = 0;
-        if (!bad && rl < T) lw = __ldg(a.la + la_base + static_cast<int64_t>(rl) * W);
-        const int nr = min(32, T - rb);
-        for (int r = 0; r < nr; ++r) {
-            const int il = rb + r;
-            const uint64_t word0 = __shfl_sync(0xffffffffu, lw, r);
-            RowWriter wr{a.kv_idx + (rowbase + t0 + il) * a.rowcap, cc, a.rowcap, lane};
-            if (il > 0)
-                for (int k = static_cast<int>(lane); k < cc; k += 32)
-                    wr.out[k] = k < kPrefixCap ? pre[k] : row0[k];
-            wr.n = c;
-            if (!bad) {
-                for (int wi = 0; 64 * wi < il; ++wi) {
-                    const uint64_t word =
-                        wi == 0 ? word0 : __ldg(a.la + la_base + static_cast<int64_t>(il) * W + wi);
-                    wr.emit(word, min(64, il - 64 * wi), t0 + 64 * wi);
-                }
-            }
-            if (lane == 0 && wr.n < a.rowcap) wr.out[wr.n] = t0 + il;
-            wr.n += 1;
-            if (lane == 0) {
-                if (wr.n > a.rowcap) bad = true;
-                a.counts[rowbase + t0 + il] = min(wr.n, a.rowcap);
-            }
+    // rows of the document, warp w taking rows w, w+4, ...: prefix, LA tiles j < il, diagonal
+    const int64_t la_base = __ldg(a.la_off + g) + (lh * T) * W;
+    const bool la_ok = la_base >= 0 && la_base + static_cast<int64_t>(T) * W <= a.la_len;
+    if (!la_ok && tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+    const int cc = min(min(c, kPrefixCap), a.rowcap);
+    for (int il = wid; il < T; il += kDecThreads / 32) {
+        RowWriter wr{rows + static_cast<int64_t>(il) * a.rowcap, c, a.rowcap, lane};
+        for (int k = static_cast<int>(lane); k < cc; k += 32) wr.out[k] = pre[k];
+        if (la_ok) {
+            for (int wi = 0; 64 * wi < il; ++wi)
+                wr.emit(__ldg(a.la + la_base + static_cast<int64_t>(il) * W + wi),
+                        min(64, il - 64 * wi), t0 + 64 * wi);
         }
+        if (lane == 0 && wr.n < a.rowcap) wr.out[wr.n] = t0 + il;
     }
-    bad = __any_sync(0xffffffffu, bad);
-    if (lane == 0 && bad) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
+}
+
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a) {
+    extern __shared__ int32_t dec_smem[];
+    if (static_cast<int>(blockIdx.x) < a.sched_blocks)
+        schedule_layer(a, blockIdx.x, dec_smem);
+    else
+        decode_segment(a, static_cast<int64_t>(blockIdx.x) - a.sched_blocks, dec_smem);
 }
 
 // one block per group: counting sort by count, descending
@@ -324,6 +496,7 @@ extern "C" sift_status sift_decode(const sift_problem *prob, const uint64_t *la_
                                    const uint64_t *ca_words, int32_t *kv_idx, int32_t *counts,
                                    int32_t *sched, int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_decode");
     sift_status st = validate_problem(prob, false);
     if (st != SIFT_OK) return st;
     if (kv_idx == nullptr || counts == nullptr || sched == nullptr || dev_status == nullptr)
@@ -343,21 +516,53 @@ extern "C" sift_status sift_decode(const sift_problem *prob, const uint64_t *la_
     a.ca_len = prob->ca_words_len;
     a.kv_idx = kv_idx;
     a.counts = counts;
+    a.sched = sched;
     a.status = dev_status;
     a.P = prob->num_prompts;
     a.D = prob->num_docs;
+    a.L = prob->num_layers;
     a.Hkv = prob->num_kv_heads;
     a.B = prob->tile;
     a.N = prob->total_tokens / prob->tile;
     a.rowcap = prob->max_tiles_per_prompt;
-    // one warp per (layer, kv head, segment), a segment being a document or a suffix
-    a.rows = static_cast<int64_t>(prob->num_layers) * a.Hkv * (a.D + a.P);
-    const int64_t blocks = (a.rows + kSegWarps - 1) / kSegWarps;
-    if (blocks > INT32_MAX) return SIFT_ERR_UNSUPPORTED;
-    decode_segments_kernel<<<static_cast<unsigned>(blocks), kSegWarps * 32, 0, stream>>>(a);
+    // one list block per (layer, kv head, segment), a segment being a document or a suffix
+    const int64_t seg_blocks = static_cast<int64_t>(a.L) * a.Hkv * (a.D + a.P);
+    // schedule blocks: hist, cap, dstart, dT, tinfo (+ the counts when they fit)
+    const size_t sched_base = (static_cast<size_t>(a.rowcap) + 1 +
+                               static_cast<size_t>(a.Hkv) * a.D + 2 * static_cast<size_t>(a.D) +
+                               static_cast<size_t>(a.N)) *
+                              sizeof(int32_t);
+    const size_t cnt_bytes = static_cast<size_t>(a.Hkv) * a.N * sizeof(int32_t);
+    const size_t list_smem = kPrefixCap * sizeof(int32_t);
+    // 227 KB per block, less the kernel's own static shared memory
+    constexpr size_t kSmemMax = 226 * 1024;
+    if (sched_base > kSmemMax) return SIFT_ERR_UNSUPPORTED;
+    a.cnt_smem = sched_base + cnt_bytes <= kSmemMax;
+    const size_t sched_smem = sched_base + (a.cnt_smem ? cnt_bytes : 0);
+    if (seg_blocks + a.L > INT32_MAX) return SIFT_ERR_UNSUPPORTED;
+    // opt in to more than the default 48 KB of dynamic shared memory only when needed
+    auto allow_smem = [](size_t bytes) {
+        return bytes <= 48 * 1024 ||
+               cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(bytes)) == cudaSuccess;
+    };
+    // one launch (the schedule blocks beside the list blocks) while the schedule's shared
+    // memory is small; otherwise the list blocks keep theirs small in a launch of their own
+    constexpr size_t kOneLaunchSmem = 32 * 1024;
+    if (sched_smem <= kOneLaunchSmem) {
+        a.sched_blocks = a.L;
+        a.seg_blocks = seg_blocks;
+        const size_t smem = sched_smem > list_smem ? sched_smem : list_smem;
+        decode_kernel<<<static_cast<unsigned>(a.L + seg_blocks), kDecThreads, smem, stream>>>(a);
+        return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
+    }
+    if (!allow_smem(sched_smem)) return SIFT_ERR_CUDA;
+    a.sched_blocks = a.L;
+    a.seg_blocks = 0;
+    decode_kernel<<<static_cast<unsigned>(a.L), kDecThreads, sched_smem, stream>>>(a);
     if (cudaGetLastError() != cudaSuccess) return SIFT_ERR_CUDA;
-    if (launch_schedule(counts, sched, prob->num_layers, a.N * a.Hkv, a.rowcap, dev_status,
-                        stream) != cudaSuccess)
-        return SIFT_ERR_CUDA;
-    return SIFT_OK;
+    a.sched_blocks = 0;
+    a.seg_blocks = seg_blocks;
+    decode_kernel<<<static_cast<unsigned>(seg_blocks), kDecThreads, list_smem, stream>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
 }

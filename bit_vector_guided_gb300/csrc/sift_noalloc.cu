@@ -91,6 +91,7 @@ extern "C" sift_status sift_dense_prefill_noalloc(const sift_problem *prob, cons
                                                   float softmax_scale, void *o, float *lse,
                                                   int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
+    NvtxRange nvtx_range("sift_dense_prefill_noalloc");
     sift_status st = validate_problem(prob, true);
     if (st != SIFT_OK) return st;
     const size_t need = sift_workspace_bytes(prob);

@@ -423,6 +423,7 @@ extern "C" sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_
                                           int32_t *qtiles, int32_t *kv, int32_t *counts,
                                           int32_t *sched, int32_t *pages, int32_t page_cap,
                                           int32_t *dev_status, cudaStream_t stream) {
+    sift::NvtxRange nvtx_range("sift_decode_ragged");
     return sift::decode_ragged_impl(prob, num_query_tiles, la_words, ca_words, qtiles, kv,
                                     counts, sched, pages, page_cap, dev_status, stream, true);
 }

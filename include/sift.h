@@ -130,7 +130,13 @@ size_t sift_workspace_bytes(const sift_problem *prob);
  *   counts  int32 [num_layers][Hkv][N]
  *   sched   int32 [num_layers][Hkv*N]: a permutation of the units
  *           u = h*N + i of each layer with non-increasing counts.
- * Bit-exact for kv_idx and counts.  Two kernel launches.
+ * Bit-exact for kv_idx and counts.  One kernel launch, in which one block per
+ * layer counts that layer's rows from the bits and sorts them while the other
+ * blocks write the lists; two launches (the same kernel, schedule blocks
+ * first) when the schedule blocks' shared memory exceeds 32 KB: (rowcap + 1 +
+ * Hkv*D + 2*D + N) x 4 bytes, plus Hkv*N x 4 for the counts when the total
+ * stays within 226 KB (rowcap = max_tiles_per_prompt, D documents).
+ * SIFT_ERR_UNSUPPORTED when the first part alone exceeds 226 KB.
  */
 sift_status sift_decode(const sift_problem *prob, const uint64_t *la_words,
                         const uint64_t *ca_words, int32_t *kv_idx, int32_t *counts,
