@@ -7,12 +7,12 @@
 // earlier documents, popcounts over each document once; the row's LA tiles; the
 // diagonal; dense rows in the suffix), then sorts the rows longest-first with a
 // counting sort in shared memory.  The other blocks write the lists, one block of
-// four warps per (layer, kv head, document or suffix): the CA prefix -- the same
-// for every row of a document -- is compacted once, by a block-wide scan over the
-// earlier documents' popcounts, then each warp takes every fourth row: the
-// prefix, its own LA tiles (each lane tests one bit; the slot is the popcount of
-// the lower lanes' bits) and the diagonal.  Both halves read only the bits, so
-// they run side by side.
+// eight warps per (layer, kv head, document or suffix): the CA prefix -- the same
+// for every row of a document -- is compacted once, by a scan over the earlier
+// documents' popcounts (one warp's shuffles up to 32 documents, the block beyond),
+// then each warp takes every eighth row: the prefix, its own LA tiles (each lane
+// tests one bit; the slot is the popcount of the lower lanes' bits) and the
+// diagonal.  Both kinds of block read only the bits, so they run side by side.
 #include <climits>
 
 #include "ptx.cuh"
@@ -106,8 +106,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
     if (lane == 31) warp_sums[wid] = incl;
     __syncthreads();
     int before = 0, all = 0;
-#pragma unroll
-    for (int w = 0; w < kDecThreads / 32; ++w) {
+    const int nw = static_cast<int>(blockDim.x >> 5);
+    for (int w = 0; w < nw; ++w) {
         const int ws = warp_sums[w];
         if (w < wid) before += ws;
         all += ws;
@@ -140,6 +140,39 @@ struct RowWriter {
     }
 };
 
+// Longest-first order of `units` counts: sched[r] = the unit with the r-th largest count
+// (ties in any order), by a counting sort in shared memory.  Counts are read from cnt and
+// clamped to [1, rowcap]; hist holds rowcap + 1 ints of shared memory.  The whole block
+// calls it.
+__device__ void sort_longest_first(const int32_t *cnt, int32_t *sched, int units, int rowcap,
+                                   int *hist, int *warp_sums) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int nb = rowcap + 1;
+    auto bin = [&](int c) { return min(max(c, 1), rowcap); };
+    for (int b = tid; b < nb; b += nt) hist[b] = 0;
+    __syncthreads();
+    for (int u = tid; u < units; u += nt) atomicAdd(&hist[bin(cnt[u])], 1);
+    __syncthreads();
+    // exclusive scan over the bins in descending count order (bin rowcap first)
+    const int per = (nb + nt - 1) / nt;
+    const int r0 = tid * per, r1 = min(r0 + per, nb);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) local += hist[rowcap - r];
+    int total = 0;
+    int run = block_exclusive_scan(local, warp_sums, &total);
+    for (int r = r0; r < r1; ++r) {
+        const int b = rowcap - r;
+        const int v = hist[b];
+        hist[b] = run;
+        run += v;
+    }
+    __syncthreads();
+    for (int u = tid; u < units; u += nt) {
+        const int pos = atomicAdd(&hist[bin(cnt[u])], 1);
+        if (pos < units) sched[pos] = u;
+    }
+}
+
 // ---- schedule blocks: every row count of layer l from the bits, then the counting sort
 // Shared memory: hist[rowcap + 1] | cap[Hkv * D] (CA prefix count of (kv head, document))
 // | dstart[D], dT[D] (first tile and tile count of each document, dT = -1 when bad)
@@ -158,7 +191,6 @@ __device__ void schedule_layer(const DecodeArgs &a, int l, int32_t *smem) {
     int *dT = dstart + a.D;
     int *tinfo = dT + a.D;
     int *cnts = tinfo + a.N;
-    for (int b = tid; b < nb; b += kDecThreads) hist[b] = 0;
     for (int i = tid; i < a.N; i += kDecThreads) tinfo[i] = kTileUnset;
     __syncthreads();
     for (int g = tid; g < a.D; g += kDecThreads) {
@@ -263,30 +295,11 @@ __device__ void schedule_layer(const DecodeArgs &a, int l, int32_t *smem) {
             }
             cnt[u] = v;
             if (a.cnt_smem) cnts[u] = v;
-            atomicAdd(&hist[v], 1);
         }
     }
     __syncthreads();
-    // exclusive scan over the bins in descending count order (bin rowcap first)
-    const int per = (nb + kDecThreads - 1) / kDecThreads;
-    const int r0 = tid * per, r1 = min(r0 + per, nb);
-    int local = 0;
-    for (int r = r0; r < r1; ++r) local += hist[a.rowcap - r];
-    int total = 0;
-    int run = block_exclusive_scan(local, warp_sums, &total);
-    for (int r = r0; r < r1; ++r) {
-        const int b = a.rowcap - r;
-        const int v = hist[b];
-        hist[b] = run;
-        run += v;
-    }
-    __syncthreads();
-    int32_t *sch = a.sched + static_cast<int64_t>(l) * U;
-    for (int u = tid; u < U; u += kDecThreads) {
-        const int c = a.cnt_smem ? cnts[u] : cnt[u];
-        const int pos = atomicAdd(&hist[c], 1);
-        if (pos < U) sch[pos] = u;
-    }
+    sort_longest_first(a.cnt_smem ? cnts : cnt, a.sched + static_cast<int64_t>(l) * U, U,
+                       a.rowcap, hist, warp_sums);
 }
 
 // ---- list blocks: all rows of one (layer, kv head, document) or one prompt's suffix
@@ -338,13 +351,13 @@ __device__ void decode_segment(const DecodeArgs &a, int64_t w, int32_t *pre) {
     const int t0 = ds / B;
     int32_t *rows = a.kv_idx + (rowbase + t0) * a.rowcap;  // row il at rows + il*rowcap
 
-    // CA prefix of the earlier documents, 128 documents per round: each thread counts one
-    // document's flagged pages, a block scan places them, each thread writes its pages
-    int c = 0;  // block-uniform
-    for (int base = g0; base < g; base += kDecThreads) {
-        const int gk = base + tid;
-        int dsk = 0, Tk = 0, cnt = 0;
-        int64_t offk = 0;
+    // CA prefix of the earlier documents: each thread counts one earlier document's flagged
+    // pages, a scan places them, each thread writes its pages.  Up to 32 earlier documents
+    // (the usual case) warp 0 does it alone with a shuffle scan; beyond, the whole block
+    // takes kDecThreads documents per round.
+    auto count_doc = [&](int gk, int &dsk, int &Tk, int64_t &offk) {
+        int cnt = 0;
+        Tk = 0;
         if (gk < g) {
             if (!doc_span(a, p, gk, dsk, Tk)) {
                 set_status(a.status, SIFT_ERR_DEVICE_CHECK);
@@ -361,8 +374,9 @@ __device__ void decode_segment(const DecodeArgs &a, int64_t w, int32_t *pre) {
                 }
             }
         }
-        int total = 0;
-        int pos = c + block_exclusive_scan(cnt, warp_sums, &total);
+        return cnt;
+    };
+    auto write_doc = [&](int pos, int dsk, int Tk, int64_t offk) {
         for (int wi = 0; 64 * wi < Tk; ++wi) {
             uint64_t word = low_bits(__ldg(a.ca + offk + wi), Tk - 64 * wi);
             while (word) {
@@ -377,11 +391,40 @@ __device__ void decode_segment(const DecodeArgs &a, int64_t w, int32_t *pre) {
                 ++pos;
             }
         }
-        c += total;
+    };
+    __shared__ int prefix_total;
+    int c = 0;  // block-uniform
+    if (g - g0 <= 32) {
+        if (wid == 0) {
+            int dsk = 0, Tk = 0;
+            int64_t offk = 0;
+            const int cnt = count_doc(g0 + static_cast<int>(lane), dsk, Tk, offk);
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (static_cast<int>(lane) >= o) incl += t;
+            }
+            write_doc(incl - cnt, dsk, Tk, offk);
+            if (lane == 31) prefix_total = incl;
+        }
+        __syncthreads();
+        c = prefix_total;
+    } else {
+        for (int base = g0; base < g; base += kDecThreads) {
+            int dsk = 0, Tk = 0;
+            int64_t offk = 0;
+            const int cnt = count_doc(base + tid, dsk, Tk, offk);
+            int total = 0;
+            const int pos = c + block_exclusive_scan(cnt, warp_sums, &total);
+            write_doc(pos, dsk, Tk, offk);
+            c += total;
+        }
+        __syncthreads();
     }
-    __syncthreads();
 
-    // rows of the document, warp w taking rows w, w+4, ...: prefix, LA tiles j < il, diagonal
+    // rows of the document, warp w taking every eighth row from w: prefix, LA tiles j < il,
+    // diagonal
     const int64_t la_base = __ldg(a.la_off + g) + (lh * T) * W;
     const bool la_ok = la_base >= 0 && la_base + static_cast<int64_t>(T) * W <= a.la_len;
     if (!la_ok && tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
@@ -406,53 +449,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const DecodeArgs a)
         decode_segment(a, static_cast<int64_t>(blockIdx.x) - a.sched_blocks, dec_smem);
 }
 
-// one block per group: counting sort by count, descending
+// one block per layer: longest-first over the layer's units
 __global__ void __launch_bounds__(1024)
 schedule_kernel(const int32_t *counts, int32_t *sched, int units, int rowcap) {
     extern __shared__ int hist[];  // rowcap + 1 bins
     __shared__ int warp_sums[32];
-    const int tid = threadIdx.x;
-    const int nb = rowcap + 1;
-    const int32_t *c = counts + static_cast<int64_t>(blockIdx.x) * units;
-    int32_t *s = sched + static_cast<int64_t>(blockIdx.x) * units;
-    for (int b = tid; b < nb; b += blockDim.x) hist[b] = 0;
-    __syncthreads();
-    for (int u = tid; u < units; u += blockDim.x) atomicAdd(&hist[min(max(c[u], 0), rowcap)], 1);
-    __syncthreads();
-    // exclusive scan over bins in descending count order (bin rowcap first)
-    const int per = (nb + blockDim.x - 1) / blockDim.x;
-    const int r0 = tid * per, r1 = min(r0 + per, nb);
-    int local = 0;
-    for (int r = r0; r < r1; ++r) local += hist[rowcap - r];
-    const int lane = tid & 31, wid = tid >> 5;
-    int incl = local;
-    for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-    }
-    if (lane == 31) warp_sums[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-        int v = lane < static_cast<int>(blockDim.x >> 5) ? warp_sums[lane] : 0;
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += t;
-        }
-        warp_sums[lane] = v;  // inclusive prefix of warp totals
-    }
-    __syncthreads();
-    int run = incl - local + (wid > 0 ? warp_sums[wid - 1] : 0);
-    for (int r = r0; r < r1; ++r) {
-        const int b = rowcap - r;
-        const int v = hist[b];
-        hist[b] = run;
-        run += v;
-    }
-    __syncthreads();
-    for (int u = tid; u < units; u += blockDim.x) {
-        const int pos = atomicAdd(&hist[min(max(c[u], 0), rowcap)], 1);
-        s[pos] = u;
-    }
+    const int64_t off = static_cast<int64_t>(blockIdx.x) * units;
+    sort_longest_first(counts + off, sched + off, units, rowcap, hist, warp_sums);
 }
 
 __global__ void dense_counts_kernel(const int32_t *cu, int P, int B, int N, int Hkv,

@@ -145,3 +145,31 @@ def plain_lists(pat, p0):
         rows.append([p0 + j for j in ca0] + [p0 + 3 + j for j in la1.get(i, [])] + [p0 + 3 + i])
     rows.append(list(range(p0, p0 + 7)))
     return rows
+
+
+def expand_lists(lay, qtiles, kv, counts, pages, layer, h):
+    """Token mask implied by the decoded lists: key c of an entry is visible to row r of
+    the query tile iff c < len, mask bit c // Pin is set and, when causal, c <= r.  Key c
+    is token first + c, or, for a gathered entry, token pages[first + c // page] + c % page
+    of the layer's page array."""
+    T, B, P = lay.total_tokens, lay.tile, lay.page_size
+    pin = min(P, B)
+    M = np.zeros((T, T), bool)
+    c = np.arange(B)
+    flat = pages[layer].reshape(-1)
+    for q, (x, rows) in enumerate(qtiles):
+        r = np.arange(rows)
+        for e in range(counts[layer, h, q]):
+            first, info = (int(v) for v in kv[layer, h, q, e])
+            ln, causal, mask = info & 0xFF, (info >> 8) & 1, (info >> 16) & 0xFFFF
+            col = (c < ln) & (((mask >> (c // pin)) & 1) == 1)
+            vis = np.broadcast_to(col[None, :], (rows, B)).copy()
+            if causal:
+                vis &= c[None, :] <= r[:, None]
+            rr, cc = np.nonzero(vis)
+            if (info >> 9) & 1:
+                keys = flat[first + cc // P] + cc % P
+            else:
+                keys = first + cc
+            M[x + rr, keys] = True
+    return M

@@ -2,7 +2,9 @@
 from its own first token, and CA pages of a size of their own.
 
 * decode: query-tile table, lists and counts bit-exact against the oracle's plain
-  ragged decode; the schedule is a longest-first permutation;
+  ragged decode, and on small layouts the key set the GPU's lists describe, expanded
+  to tokens, equal to the token-level rule; the schedule is a longest-first
+  permutation;
 * attention: every row against the oracle (fp64, key set read from the bits), within
   the tolerances of the aligned path;
 * on an aligned layout the general path issues the same MMAs in the same order as the
@@ -20,7 +22,7 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import assert_attention_close, check_sched, device_bits
+from helpers import assert_attention_close, check_sched, device_bits, expand_lists
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +62,15 @@ def _check_decode(sift, lay, la, ca, prob, la_d, ca_d):
                 n = cnt_h[l, h, q]
                 assert np.array_equal(kv_h[l, h, q, :n], kv_o[l, h, q, :n]), (l, h, q)
     check_sched(sched.cpu().numpy(), cnt_h)
+    if lay.total_tokens <= 6000:
+        # beyond the encoding: the key set the GPU's own lists describe, expanded to tokens,
+        # is the token-level rule written out block by block (oracle.token_mask)
+        pg_e = pages.cpu().numpy() if pages is not None else np.zeros((L, H, 1, 1), np.int32)
+        qt_h = qt.cpu().numpy()
+        for l in range(L):
+            for h in range(H):
+                got = expand_lists(lay, qt_h, kv_h, cnt_h, pg_e, l, h)
+                assert np.array_equal(got, oracle.token_mask(lay, la, ca, l, h)), (l, h)
     if pages is not None:  # gathered pages: every page a list points at, bit-exact
         pg_h = pages.cpu().numpy()
         for l in range(L):
