@@ -75,6 +75,13 @@ EDGE_CFGS = [
                     num_layers=1, num_q_heads=2, num_kv_heads=1, head_dim=64, tile=64),
     W.custom_config("dec_zeros", [([256] * 3, 128)], W.BitSpec(pattern="zeros"),
                     num_layers=1, num_q_heads=2, num_kv_heads=1, head_dim=64, tile=64),
+    # 40 kv heads x 1,360 query tiles = 54,400 rows in one layer: the schedule block's
+    # counts no longer fit in shared memory beside its tables, so its sort reads them
+    # back from the counts array (the batch-of-4 and 262K workloads cover the two-launch
+    # form, the 33K one the single launch with the counts in shared memory)
+    W.custom_config("dec_many_rows", [([64 * 40] * 34, 0)],
+                    W.BitSpec(la_p=0.2, ca_p=0.05, ca_first_page=True), num_layers=1,
+                    num_q_heads=80, num_kv_heads=40, head_dim=64, tile=64),
 ]
 
 
