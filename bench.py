@@ -513,6 +513,9 @@ def run_ours(args, cfg):
         # schedule written once (counts read back by the schedule)
         "decode_gbs": decode_bytes(lay, counts_h) / (float(np.median(decode_ms)) * 1e-3) / 1e9,
         "decode_bytes": decode_bytes(lay, counts_h),
+        "decode_note": "decode_gbs: algorithmic bytes over CUDA-event time; the launch's "
+                       "duration and DRAM bytes from ncu are in "
+                       "profiles/sift_decode_llama_32k.md (the lists stay in L2)",
         # diagonal tiles counted at the (B+1)/(2B) of their entries that are causal
         "useful_tflops": value * useful_fraction(cfg, lay, flops_step),
         "fused_ms_per_step": fused_ms_step,
