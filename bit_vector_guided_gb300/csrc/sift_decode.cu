@@ -71,14 +71,18 @@ __device__ __forceinline__ uint64_t low_bits(uint64_t word, int nb) {
 }
 
 // Document g of prompt p: first token ds and tile count T; false when its bounds are
-// inconsistent (not multiples of B, empty, outside the prompt)
+// inconsistent (not multiples of B, empty, outside the prompt or the batch)
 __device__ __forceinline__ bool doc_span(const DecodeArgs &a, int p, int g, int &ds, int &T) {
     const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
     const int g0 = __ldg(a.doc_cu + p);
-    ds = (g == g0) ? p0 : __ldg(a.doc_end + g - 1);
-    const int de = __ldg(a.doc_end + g);
     T = 0;
-    if (p0 % a.B || ds % a.B || de % a.B || de <= ds || ds < p0 || de > p1) return false;
+    ds = p0;
+    if (g0 < 0 || g < g0 || g >= a.D || p0 < 0) return false;
+    if (g > g0) ds = __ldg(a.doc_end + g - 1);
+    const int de = __ldg(a.doc_end + g);
+    if (p0 % a.B || ds % a.B || de % a.B || de <= ds || ds < p0 || de > p1 ||
+        static_cast<int64_t>(de) > static_cast<int64_t>(a.N) * a.B)
+        return false;
     T = (de - ds) / a.B;
     return true;
 }
@@ -200,14 +204,15 @@ __device__ void schedule_layer(const DecodeArgs &a, int l, int32_t *smem) {
         if (!ok) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
         dstart[g] = ds / a.B;
         dT[g] = ok ? T : -1;
-        for (int r = 0; r < T; ++r) tinfo[ds / a.B + r] = g;
+        for (int r = 0; r < T; ++r) tinfo[ds / a.B + r] = g;  // T > 0 only inside [0, N)
     }
     for (int p = tid; p < a.P; p += kDecThreads) {
         const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
         const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
         int sstart = p0;
         if (g0 >= 0 && g0 < g1 && g1 <= a.D) sstart = __ldg(a.doc_end + g1 - 1);
-        if (p0 % a.B || p1 % a.B || sstart % a.B || sstart < p0 || sstart > p1 || p1 > a.N * a.B) {
+        if (p0 % a.B || p1 % a.B || p0 < 0 || sstart % a.B || sstart < p0 || sstart > p1 ||
+            static_cast<int64_t>(p1) > static_cast<int64_t>(a.N) * a.B) {
             set_status(a.status, SIFT_ERR_DEVICE_CHECK);
             continue;
         }
@@ -319,7 +324,8 @@ __device__ void decode_segment(const DecodeArgs &a, int64_t w, int32_t *pre) {
         const int p = seg - a.D;
         const int p0 = __ldg(a.cu + p), p1 = __ldg(a.cu + p + 1);
         const int g0 = __ldg(a.doc_cu + p), g1 = __ldg(a.doc_cu + p + 1);
-        if (p0 % B || p1 % B || p0 > p1 || g0 < 0 || g0 > g1 || g1 > a.D) {
+        if (p0 % B || p1 % B || p0 < 0 || p0 > p1 || g0 < 0 || g0 > g1 || g1 > a.D ||
+            static_cast<int64_t>(p1) > static_cast<int64_t>(a.N) * B) {
             if (tid == 0) set_status(a.status, SIFT_ERR_DEVICE_CHECK);
             return;
         }

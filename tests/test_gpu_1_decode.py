@@ -153,6 +153,29 @@ def test_decode_device_check_on_bad_offsets(sift):
     assert int(st.item()) == 5  # SIFT_ERR_DEVICE_CHECK
 
 
+def test_decode_device_check_on_prompt_past_the_batch(sift):
+    """A prompt end past total_tokens (cu_seqlens lives on the device, so only the kernel
+    can see it) is reported; the kernel bounds every index by the batch's tiles."""
+    cfg = EDGE_CFGS[0]
+    lay = W.make_layout(cfg)
+    la, ca = W.make_bits(cfg, lay)
+    cu = lay.cu_seqlens.copy()
+    cu[-1] = lay.total_tokens + 4 * lay.tile
+    prob = sift.SiftProblem(cu_seqlens=cu, doc_cu=lay.doc_cu, doc_end=lay.doc_end,
+                            la_off=lay.la_off, ca_off=lay.ca_off, num_layers=lay.num_layers,
+                            num_q_heads=lay.num_q_heads, num_kv_heads=lay.num_kv_heads,
+                            head_dim=lay.head_dim, tile=lay.tile, la_words_len=lay.la_words_len,
+                            ca_words_len=lay.ca_words_len,
+                            max_tiles_per_prompt=lay.max_tiles_per_prompt)
+    # the struct the kernel reads keeps the batch's real size; only the device array lies
+    prob._struct.total_tokens = lay.total_tokens
+    la_d, ca_d = device_bits(la, ca)
+    st = prob.new_status()
+    sift.decode(prob, la_d, ca_d, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5  # SIFT_ERR_DEVICE_CHECK
+
+
 def test_decode_rejects_bad_arguments(sift):
     lay, la, ca, prob, la_d, ca_d = setup(EDGE_CFGS[0])
     with pytest.raises(sift.SiftError) as e:
