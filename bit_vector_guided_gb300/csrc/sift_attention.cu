@@ -10,15 +10,19 @@
 //
 // One work item = (query tile i, kv head h, pair of query heads of h's group).
 // Both heads of the pair share every K/V tile staged in shared memory, and the
-// decoded list of row (h, i).  Roles inside the 352-thread CTA:
-//   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane)
-//   warps 4-7  softmax of head slot 1
-//   warp  8    scheduler + K producer (K_j into a 3-slot ring; K is consumed first, so it
-//              gets the deeper prefetch); it claims the next item early and pulls that
-//              item's Q into L2, and runs ahead into the next item's K tiles
+// decoded list of row (h, i).  Roles inside the 384-thread CTA:
+//   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane); after the item's
+//              last tile, its epilogue: O / l in bf16 into the shared-memory staging tile
+//              (general layout: straight to global memory, row by row)
+//   warps 4-7  softmax of head slot 1, the same
+//   warp  8    scheduler + K producer (K_j into a ring of 2 slots, 3 on the general
+//              layout); it claims the next item early and pulls that item's Q into L2, and
+//              runs ahead into its K tiles
 //   warp  9    TMEM allocator + MMA issuer (warp-wide loop, one elected lane issues)
 //   warp 10    Q + V producer (the item's Q pair once the previous one is released, then
 //              V_j into a 2-slot ring)
+//   warp 11    O writer: one TMA store per staged head tile, then hands the staging tile
+//              back once the store has read it (idle on the general layout)
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
 // P*V MMA reads it from tensor memory, so P never touches shared memory.
@@ -42,12 +46,18 @@
 namespace sift {
 namespace {
 
-constexpr int kThreads = 352;
+// threads of a CTA: 12 warps, or 11 on the general layout (no O writer)
+constexpr int threads_for(bool staged) { return staged ? 384 : 352; }
 constexpr int kProducerWarp = 8;   // scheduler and K loads
 constexpr int kMmaWarp = 9;        // TMEM allocator and MMA issuer
 constexpr int kVProducerWarp = 10; // Q and V loads
-constexpr int kKSlots = 3;  // K ring: K_j is consumed first, so it gets the deeper ring
-constexpr int kVSlots = 2;  // V ring
+constexpr int kStoreWarp = 11;     // TMA stores of O
+// K ring: three slots on the general layout; two elsewhere, where the shared memory of the
+// third holds the staging tile of O instead (measured on aligned rows: the third K slot
+// was worth nothing, the staged O stores 1.5%; on the general layout, whose gathered pages
+// keep the copy engine busier, the TMA stores cost 5%).  V ring: two slots.
+constexpr int kKSlotsMax = 3;
+constexpr int kVSlots = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all of TMEM)
@@ -83,8 +93,11 @@ struct Ctl {
     // per head slot: a slot's Q for the next item loads as soon as this item's last S of
     // that head is done (head 0's a step before head 1's)
     uint64_t q_full[2], q_empty[2];
-    uint64_t k_full[kKSlots], k_empty[kKSlots], v_full[kVSlots], v_empty[kVSlots];
+    uint64_t k_full[kKSlotsMax], k_empty[kKSlotsMax], v_full[kVSlots], v_empty[kVSlots];
     uint64_t s_full[2], p_full[2], o_full[2];
+    // the O staging tile, used by head 0 and head 1 in turn: stage_full[s] when head s has
+    // written it, stage_free[s] when the TMA store of head s's tile has read it
+    uint64_t stage_full[2], stage_free[2];
     uint64_t sch_full[2], sch_empty[2];
     uint64_t teardown, never;
     WorkItem items[2];
@@ -126,8 +139,9 @@ struct AttnParams {
 
 constexpr uint32_t kGatherBit = 1u << 9;  // list entry of gathered pages (general layout)
 
-template <int BT, int HD>
+template <int BT, int HD, bool STAGED>
 struct Geo {
+    static constexpr int kKSlots = STAGED ? 2 : 3;
     static constexpr int kBoxes = HD / 64;          // 64-column (128-byte) swizzled boxes
     static constexpr int kQBox = 128 * 128;          // bytes: 128 rows (MMA M) x 128 B
     static constexpr int kQBytes = 2 * kBoxes * kQBox;
@@ -135,7 +149,9 @@ struct Geo {
     static constexpr int kKVBytes = kBoxes * kKVBox;
     static constexpr int kKOff = kQBytes;
     static constexpr int kVOff = kKOff + kKSlots * kKVBytes;
-    static constexpr int kCtlOff = kVOff + kVSlots * kKVBytes;
+    static constexpr int kOBox = BT * 128;                 // bytes: tile rows x 128 B
+    static constexpr int kOOff = kVOff + kVSlots * kKVBytes;  // O staging tile, kBoxes boxes
+    static constexpr int kCtlOff = kOOff + (STAGED ? kBoxes * kOBox : 0);
     static constexpr int kSmemUsed = kCtlOff + 1024 + 1024;  // + control block + align slack
     static constexpr int kSmem = kSmemUsed > kMinSmem ? kSmemUsed : kMinSmem;
     static constexpr uint32_t kTxQ = 2 * kBoxes * BT * 128;
@@ -464,13 +480,19 @@ __device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int 
 }
 
 template <int BT, int HD, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(MODE != kModeRagged), 1)
 sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                       const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV,
                       const __grid_constant__ CUtensorMap tmKp,  // page-high boxes (gather)
-                      const __grid_constant__ CUtensorMap tmVp, const AttnParams p) {
-    using G = Geo<BT, HD>;
+                      const __grid_constant__ CUtensorMap tmVp,
+                      const __grid_constant__ CUtensorMap tmO,  // O, tile-high boxes (stores)
+                      const AttnParams p) {
+    // whole tiles go out through a shared-memory staging tile and TMA stores, except on the
+    // general layout (rows written by their softmax threads)
+    constexpr bool STAGED = MODE != kModeRagged;
+    using G = Geo<BT, HD, STAGED>;
+    constexpr int kKSlots = G::kKSlots;
     constexpr bool DENSE = MODE == kModeDense;
     constexpr bool RAGGED = MODE == kModeRagged;  // list entries are first tokens, not tiles
     (void)DENSE;
@@ -482,6 +504,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     const uint32_t q_s = sbase;
     const uint32_t k_s = sbase + G::kKOff;
     const uint32_t v_s = sbase + G::kVOff;
+    const uint32_t o_s = sbase + G::kOOff;
     Ctl &c = *reinterpret_cast<Ctl *>(smem + G::kCtlOff);
 
     const int warp = threadIdx.x >> 5;
@@ -507,7 +530,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             ptx::mbar_init(B_(c.p_full[s]), G::kSoftWarps);
             ptx::mbar_init(B_(c.o_full[s]), 1);
             ptx::mbar_init(B_(c.sch_full[s]), 1);
-            ptx::mbar_init(B_(c.sch_empty[s]), 2 + 2 * G::kSoftWarps);
+            // V producer, MMA issuer, the O writer (when staged), softmax warps of both heads
+            ptx::mbar_init(B_(c.sch_empty[s]), (STAGED ? 3 : 2) + 2 * G::kSoftWarps);
+        }
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(B_(c.stage_full[s]), G::kSoftWarps);
+            ptx::mbar_init(B_(c.stage_free[s]), 1);
         }
         ptx::mbar_init(B_(c.teardown), 1);
         ptx::mbar_init(B_(c.never), 1);
@@ -532,6 +560,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         ptx::prefetch_tmap(&tmQ);
         ptx::prefetch_tmap(&tmK);
         ptx::prefetch_tmap(&tmV);
+        ptx::prefetch_tmap(&tmO);
         if (RAGGED) {
             ptx::prefetch_tmap(&tmKp);
             ptx::prefetch_tmap(&tmVp);
@@ -890,7 +919,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             drain_bar(B_(c.teardown), 0, p.timeout_ns);
         }
         __syncwarp();
-    } else {
+    } else if (warp < kProducerWarp) {
         // ------------------------------------------------ softmax + epilogue
         const int s = warp >> 2;
         const int wq = warp & 3;
@@ -909,6 +938,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             // and the first warp of head slot 0 hands back that slot's Q after its last S
             const bool q0_releaser = (s == 0 && wq == 0 && lane == 0);
             int t = 0;  // key tiles seen so far, same order as the producers and the MMA issuer
+            int n_staged = 0;  // this head's tiles written through the staging tile so far
             while (true) {
                 const int slot = item_k & 1;
                 if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
@@ -1002,6 +1032,20 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 oph ^= 1;
                 if (releaser) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
                 ptx::tc_fence_after();
+                // Aligned tiles go through the staging tile and one TMA store per box; the
+                // general layout's tiles are written row by row (a partial one must not spill
+                // into the next segment, and the stores would compete with its gathered page
+                // loads).  The heads take the staging tile in turn: head 0's m-th tile after
+                // head 1's (m-1)-th has been read, head 1's after head 0's m-th.
+                const bool staged = STAGED;
+                if (staged) {
+                    bool free_ok = true;
+                    if (s == 0 && n_staged > 0)
+                        free_ok = wait_warp(c, B_(c.stage_free[1]), (n_staged - 1) & 1, p);
+                    else if (s == 1)
+                        free_ok = wait_warp(c, B_(c.stage_free[0]), n_staged & 1, p);
+                    if (!free_ok) break;
+                }
                 const float inv = 1.f / l;
                 const int64_t tok = RAGGED ? static_cast<int64_t>(it.q0) + row
                                            : static_cast<int64_t>(it.i) * BT + row;
@@ -1010,6 +1054,9 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 // rows past the segment's end are not stored; every lane still takes part
                 // in the warp-collective tensor-memory loads
                 const bool store = !RAGGED || row < it.qlen;
+                // this row in the staging tile: box cc/2, 128 bytes per row, 16-byte chunks
+                // placed by the 128-byte swizzle (chunk k of row r at k ^ (r % 8))
+                const uint32_t srow = o_s + static_cast<uint32_t>(row) * 128u;
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     float ov[32];
@@ -1018,7 +1065,15 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
 #pragma unroll
                     for (int t = 0; t < 16; ++t)
                         pk[t] = ptx::pack_bf16x2(ov[2 * t] * inv, ov[2 * t + 1] * inv);
-                    if (store) {
+                    if (staged) {
+                        const uint32_t box = srow + static_cast<uint32_t>(cc >> 1) * G::kOBox;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint32_t chunk = static_cast<uint32_t>((cc & 1) * 4 + k);
+                            ptx::st_shared_v4(box + ((chunk ^ static_cast<uint32_t>(row & 7)) << 4),
+                                              pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+                        }
+                    } else if (store) {
                         if (p.o_v8) {  // whole 32-byte sectors: half the store instructions
                             ptx::st_global_v8(orow + cc * 4, pk);
                             ptx::st_global_v8(orow + cc * 4 + 2, pk + 8);
@@ -1030,12 +1085,55 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         }
                     }
                 }
+                if (staged) {
+                    ptx::fence_proxy_async_smem();  // the TMA store reads what these threads wrote
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(B_(c.stage_full[s]));
+                    ++n_staged;
+                }
                 if (store)
                     p.lse[static_cast<int64_t>(hq) * p.total_tokens + tok] =
                         (m + log2f(l)) * 0.69314718055994530942f;
                 ptx::tc_fence_before();
             }
         }
+    } else if (STAGED && warp == kStoreWarp) {
+        // ------------------------------------------------ O writer
+        // Follows the items; for each whole tile, head 0's then head 1's staged O goes out
+        // as one TMA store per 64-column box (one lane per box), and the staging tile is
+        // handed back once the store has read it.
+        int item_k = 0, n = 0;
+        bool issued = false;
+        while (true) {
+            const int slot = item_k & 1;
+            if (!wait_warp(c, B_(c.sch_full[slot]), (item_k >> 1) & 1, p)) break;
+            const WorkItem it = c.items[slot];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(B_(c.sch_empty[slot]));
+            ++item_k;
+            if (!it.valid) break;
+            const int tok0 = RAGGED ? it.q0 : it.i * BT;
+            bool ok = true;
+            for (int s = 0; s < 2; ++s) {
+                if (!wait_warp(c, B_(c.stage_full[s]), n & 1, p)) {
+                    ok = false;
+                    break;
+                }
+                if (static_cast<int>(lane) < G::kBoxes) {
+                    ptx::tma_store_3d(&tmO, o_s + lane * G::kOBox, 64 * lane, it.hq0 + s, tok0);
+                    ptx::bulk_commit();
+                    ptx::bulk_wait_read();
+                    issued = true;
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(B_(c.stage_free[s]));
+            }
+            if (!ok) break;
+            ++n;
+        }
+        // every store must have landed before the kernel ends
+        if (issued) ptx::bulk_wait_all();
+        __syncwarp();
     }
 
     ptx::tc_fence_before();
@@ -1084,9 +1182,9 @@ bool make_map(CUtensorMap *m, const void *base, int d, int heads, int tokens, in
 
 template <int BT, int HD, int MODE>
 sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const CUtensorMap &mv,
-                             const CUtensorMap &mkp, const CUtensorMap &mvp, const AttnParams &p,
-                             cudaStream_t stream) {
-    using G = Geo<BT, HD>;
+                             const CUtensorMap &mkp, const CUtensorMap &mvp, const CUtensorMap &mo,
+                             const AttnParams &p, cudaStream_t stream) {
+    using G = Geo<BT, HD, MODE != kModeRagged>;
     auto kern = sift_attention_kernel<BT, HD, MODE>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -1099,23 +1197,24 @@ sift_status launch_attention(const CUtensorMap &mq, const CUtensorMap &mk, const
     if (sms <= 0) return SIFT_ERR_CUDA;
     const int grid = p.total_items < sms ? p.total_items : sms;
     if (grid <= 0) return SIFT_OK;
-    kern<<<grid, kThreads, G::kSmem, stream>>>(mq, mk, mv, mkp, mvp, p);
+    kern<<<grid, threads_for(MODE != kModeRagged), G::kSmem, stream>>>(mq, mk, mv, mkp, mvp, mo, p);
     return cudaGetLastError() == cudaSuccess ? SIFT_OK : SIFT_ERR_CUDA;
 }
 
 // maps: Q, K, V with tile-high boxes, then K, V with page-high boxes (gathered pages of
-// the general layout; the tile-high ones again everywhere else)
+// the general layout; the tile-high ones again everywhere else), then O with tile-high
+// boxes (stores)
 template <int MODE>
 sift_status dispatch(int tile, int hd, const CUtensorMap *m, const AttnParams &p,
                      cudaStream_t stream) {
     if (tile == 128 && hd == 128)
-        return launch_attention<128, 128, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+        return launch_attention<128, 128, MODE>(m[0], m[1], m[2], m[3], m[4], m[5], p, stream);
     if (tile == 128 && hd == 64)
-        return launch_attention<128, 64, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+        return launch_attention<128, 64, MODE>(m[0], m[1], m[2], m[3], m[4], m[5], p, stream);
     if (tile == 64 && hd == 128)
-        return launch_attention<64, 128, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+        return launch_attention<64, 128, MODE>(m[0], m[1], m[2], m[3], m[4], m[5], p, stream);
     if (tile == 64 && hd == 64)
-        return launch_attention<64, 64, MODE>(m[0], m[1], m[2], m[3], m[4], p, stream);
+        return launch_attention<64, 64, MODE>(m[0], m[1], m[2], m[3], m[4], m[5], p, stream);
     return SIFT_ERR_UNSUPPORTED;
 }
 
@@ -1141,6 +1240,7 @@ sift_status prepare(const sift_problem *prob, const void *q, const void *k, cons
         return SIFT_ERR_CUDA;
     maps[3] = maps[1];
     maps[4] = maps[2];
+    if (!make_map(&maps[5], o, d, prob->num_q_heads, T, B)) return SIFT_ERR_CUDA;
     const int N = num_query_tiles > 0 ? num_query_tiles : T / B;
     const int G = prob->num_q_heads / prob->num_kv_heads;
     AttnParams a{};
@@ -1182,7 +1282,7 @@ extern "C" sift_status sift_sparse_prefill(const sift_problem *prob, int32_t lay
     if (prob == nullptr || layer < 0 || layer >= prob->num_layers || kv_idx == nullptr ||
         counts == nullptr || sched == nullptr)
         return SIFT_ERR_INVALID_ARG;
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
@@ -1216,7 +1316,7 @@ extern "C" sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int3
         return SIFT_ERR_INVALID_ARG;
     if (validate_ragged(prob, true) == SIFT_OK && num_query_tiles > max_query_tiles(prob))
         return SIFT_ERR_INVALID_ARG;
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p, num_query_tiles);
@@ -1258,7 +1358,7 @@ extern "C" sift_status sift_dense_prefill(const sift_problem *prob, const void *
                                           int32_t *dev_status, cudaStream_t stream) {
     using namespace sift;
     NvtxRange nvtx_range("sift_dense_prefill");
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
@@ -1290,7 +1390,7 @@ extern "C" sift_status sift_fused_prefill(const sift_problem *prob, int32_t laye
         (prob->ca_words_len > 0 && ca_words == nullptr))
         return SIFT_ERR_INVALID_ARG;
     if (prob->num_prompts > kMaxFusedPrompts) return SIFT_ERR_UNSUPPORTED;
-    CUtensorMap maps[5];
+    CUtensorMap maps[6];
     AttnParams p;
     sift_status st = prepare(prob, q, k, v, softmax_scale, o, lse, workspace, workspace_bytes,
                              dev_status, maps, &p);
