@@ -94,7 +94,8 @@ struct Ctl {
     // that head is done (head 0's a step before head 1's)
     uint64_t q_full[2], q_empty[2];
     uint64_t k_full[kKSlotsMax], k_empty[kKSlotsMax], v_full[kVSlots], v_empty[kVSlots];
-    uint64_t s_full[2], p_full[2], o_full[2];
+    // p_half[s]: the first half of head s's P (keys [0, B/2)) is in tensor memory
+    uint64_t s_full[2], p_half[2], p_full[2], o_full[2];
     // the O staging tile, used by head 0 and head 1 in turn: stage_full[s] when head s has
     // written it, stage_free[s] when the TMA store of head s's tile has read it
     uint64_t stage_full[2], stage_free[2];
@@ -439,10 +440,27 @@ __device__ bool walk_bits(const AttnParams &p, const WorkItem &it, uint32_t lane
     return visit(it.i);
 }
 
+// Columns c >= lim of a key tile are cleared (to -inf), 32 at a time: a word wholly below
+// lim is left alone, one wholly at or above it is overwritten without tests, and only the
+// word that holds lim compares column by column.
+template <int BT>
+__device__ __forceinline__ void mask_from(float (&x)[BT], int lim) {
+#pragma unroll
+    for (int w = 0; w < BT / 32; ++w) {
+        const int c0 = 32 * w;
+        if (lim < c0 + 32) {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[c0 + t] = c0 + t < lim ? x[c0 + t] : -INFINITY;
+        }
+    }
+}
+
 // General layout: clear (to -inf) the columns of a key tile that row `row` may not use.
 // info = len | causal << 8 | mask << 16: columns c < len whose page bit c >> lp is set,
-// and c <= row on the diagonal.  One 32-column visibility word at a time; words that
-// are wholly visible (most of them) skip the selects.
+// and c <= row on the diagonal.  When every page under the first len columns is kept
+// (diagonal tiles, a partial last group of gathered pages, a partial last page) the
+// visible columns are a prefix and one limit per row describes them; otherwise one
+// 32-column visibility word at a time, words that are wholly visible skipping the selects.
 __device__ __forceinline__ uint32_t page_word(uint32_t pm, int w, int lp) {
     if (lp >= 5) return ((pm >> ((32 * w) >> lp)) & 1u) ? kFull : 0u;  // one page per word
     if (lp == 4) {  // 2 pages of 16 columns: bit k -> bits [16k, 16k+16)
@@ -465,6 +483,12 @@ __device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int 
     const int len = static_cast<int>(info & 0xffu);
     const bool causal = (info >> 8) & 1u;
     const uint32_t pm = info >> 16;
+    const int np = min((len + (1 << lp) - 1) >> lp, BT >> lp);  // pages under [0, len)
+    const uint32_t need = (1u << np) - 1u;
+    if ((pm & need) == need) {
+        mask_from<BT>(x, causal ? min(len, row + 1) : len);
+        return;
+    }
 #pragma unroll
     for (int w = 0; w < BT / 32; ++w) {
         const int c0 = 32 * w;
@@ -527,6 +551,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(B_(c.s_full[s]), 1);
+            ptx::mbar_init(B_(c.p_half[s]), G::kSoftWarps);
             ptx::mbar_init(B_(c.p_full[s]), G::kSoftWarps);
             ptx::mbar_init(B_(c.o_full[s]), 1);
             ptx::mbar_init(B_(c.sch_full[s]), 1);
@@ -809,18 +834,31 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     if (ptx::elect_one()) ptx::umma_ss_c<true>(d, qa + off_q, kb + off_k, G::kIdescS);
                 }
             };
-            auto issue_pv = [&](int s, int vslot, bool acc) {
+            // P*V of head s: the MMAs over the first half of the keys go out as soon as that
+            // half of P is in tensor memory, while the softmax still works on the second
+            auto issue_pv = [&](int s, int vslot, bool acc) -> bool {
                 const uint64_t vb = dv + static_cast<uint32_t>((vslot * G::kKVBytes) >> 4);
                 const uint32_t d = s ? tO1 : tO0;
                 const uint32_t a = s ? tS1 : tS0;
+                uint32_t &ph = s ? pph1 : pph0;
+                if (!wait_warp(c, B_(c.p_half[s]), ph, p)) return false;
+                ptx::tc_fence_after();
                 if (ptx::elect_one()) {
                     if (acc) ptx::umma_ts_c<true>(d, a, vb, G::kIdescPV);
                     else ptx::umma_ts_c<false>(d, a, vb, G::kIdescPV);
                 }
 #pragma unroll
-                for (int kk = 1; kk < BT / 16; ++kk)
+                for (int kk = 1; kk < BT / 32; ++kk)
                     if (ptx::elect_one())
                         ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
+                if (!wait_warp(c, B_(c.p_full[s]), ph, p)) return false;
+                ph ^= 1;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int kk = BT / 32; kk < BT / 16; ++kk)
+                    if (ptx::elect_one())
+                        ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
+                return true;
             };
             // An item's last P*V pair (the "tail") completes its O.  General layout: the
             // pattern runs on across the item boundary, each head's tail issued right before
@@ -832,16 +870,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             bool tail = false, ok = true;
             int tail_n = 0;
             auto issue_tail = [&]() -> bool {
-                if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !wait_warp(c, B_(c.p_full[0]), pph0, p))
+                if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, tail_n > 1))
                     return false;
-                pph0 ^= 1;
-                ptx::tc_fence_after();
-                issue_pv(0, vs, tail_n > 1);
                 commit(B_(c.o_full[0]));
-                if (!wait_warp(c, B_(c.p_full[1]), pph1, p)) return false;
-                pph1 ^= 1;
-                ptx::tc_fence_after();
-                issue_pv(1, vs, tail_n > 1);
+                if (!issue_pv(1, vs, tail_n > 1)) return false;
                 commit(B_(c.o_full[1]));
                 return true;
             };
@@ -871,24 +903,17 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const bool pv = j > 0 || tail;
                     const bool pv_acc = j > 0 ? j > 1 : tail_n > 1;
                     if (pv) {
-                        if (!wait_warp(c, B_(c.v_full[vs]), vph, p) ||
-                            !wait_warp(c, B_(c.p_full[0]), pph0, p)) {
+                        if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, pv_acc)) {
                             ok = false;
                             break;
                         }
-                        pph0 ^= 1;
-                        ptx::tc_fence_after();
-                        issue_pv(0, vs, pv_acc);
                         if (j == 0) commit(B_(c.o_full[0]));
                     }
                     if (kCarry && !wait_qk(j)) { ok = false; break; }
                     issue_s(0, ks);
                     commit(B_(c.s_full[0]));
                     if (pv) {
-                        if (!wait_warp(c, B_(c.p_full[1]), pph1, p)) { ok = false; break; }
-                        pph1 ^= 1;
-                        ptx::tc_fence_after();
-                        issue_pv(1, vs, pv_acc);
+                        if (!issue_pv(1, vs, pv_acc)) { ok = false; break; }
                         if (j == 0) commit(B_(c.o_full[1]));
                     }
                     if (j == 0) {  // head 1's Q of this item
@@ -968,9 +993,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     if constexpr (RAGGED) {
                         if ((info & ~kGatherBit) != p.full_info) mask_columns<BT>(x, info, row, p.lp);
                     } else if (j == it.n - 1) {
-#pragma unroll
-                        for (int cidx = 0; cidx < BT; ++cidx)
-                            if (cidx > row) x[cidx] = -INFINITY;
+                        mask_from<BT>(x, row + 1);  // the diagonal tile: keys up to the row's own
                     }
                     // row max: independent three-input chains of 32 columns each
                     float mxc[BT / 32];
@@ -991,7 +1014,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         alpha = ptx::ex2(m - m_new);
                         m = m_new;
                     }
-                    // p = 2^(x*scale*log2e - m): packed FMA, MUFU ex2, packed partial sums
+                    // p = 2^(x*scale*log2e - m): packed FMA, MUFU ex2, packed partial sums.
+                    // Each half of the keys is handed to the MMA issuer as soon as it is stored.
                     const uint64_t sl2x2 = ptx::f2(sl2, sl2);
                     const uint64_t nmb = ptx::f2(-m, -m);
                     uint64_t acc[4];
@@ -999,33 +1023,41 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     for (int q = 0; q < 4; ++q) acc[q] = ptx::f2(0.f, 0.f);
                     uint32_t pk[BT / 2];
 #pragma unroll
-                    for (int t = 0; t < BT / 2; ++t) {
-                        float e0, e1;
-                        ptx::f2_split(ptx::ffma2(ptx::f2(x[2 * t], x[2 * t + 1]), sl2x2, nmb), e0, e1);
-                        const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
-                        acc[t & 3] = ptx::fadd2(acc[t & 3], ptx::f2(p0, p1));
-                        pk[t] = ptx::pack_bf16x2(p0, p1);
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int t = h * (BT / 4); t < (h + 1) * (BT / 4); ++t) {
+                            float e0, e1;
+                            ptx::f2_split(ptx::ffma2(ptx::f2(x[2 * t], x[2 * t + 1]), sl2x2, nmb), e0, e1);
+                            const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                            acc[t & 3] = ptx::fadd2(acc[t & 3], ptx::f2(p0, p1));
+                            pk[t] = ptx::pack_bf16x2(p0, p1);
+                        }
+                        const uint32_t(&half)[BT / 4] =
+                            *reinterpret_cast<const uint32_t(*)[BT / 4]>(pk + h * (BT / 4));
+                        if constexpr (BT == 128) ptx::tmem_st32(tS + h * 32, half);
+                        else ptx::tmem_st16(tS + h * 16, half);
+                        // O takes the new max before any of this tile's P reaches the tensor
+                        // pipe (this head's P*V of the previous tile finished before its S did)
+                        if (h == 0 && j > 0 && __any_sync(kFull, need)) {
+#pragma unroll 1
+                            for (int cc = 0; cc < HD / 32; ++cc) {
+                                float ov[32];
+                                ptx::tmem_ld32(tO + cc * 32, ov);
+#pragma unroll
+                                for (int t = 0; t < 32; ++t) ov[t] *= alpha;
+                                ptx::tmem_st32f(tO + cc * 32, ov);
+                            }
+                        }
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(B_(h == 0 ? c.p_half[s] : c.p_full[s]));
                     }
-                    if constexpr (BT == 128) ptx::tmem_st64(tS, pk); else ptx::tmem_st32(tS, pk);
                     {
                         float a0, a1;
                         ptx::f2_split(ptx::fadd2(ptx::fadd2(acc[0], acc[1]), ptx::fadd2(acc[2], acc[3])),
                                       a0, a1);
                         l = l * alpha + (a0 + a1);
                     }
-                    if (j > 0 && __any_sync(kFull, need)) {
-#pragma unroll 1
-                        for (int cc = 0; cc < HD / 32; ++cc) {
-                            float ov[32];
-                            ptx::tmem_ld32(tO + cc * 32, ov);
-#pragma unroll
-                            for (int t = 0; t < 32; ++t) ov[t] *= alpha;
-                            ptx::tmem_st32f(tO + cc * 32, ov);
-                        }
-                    }
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(B_(c.p_full[s]));
                 }
                 if (!ok) break;
                 if (!wait_warp(c, B_(c.o_full[s]), oph, p)) break;
