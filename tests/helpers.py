@@ -41,6 +41,23 @@ def check_sched(sched, counts):
         assert np.all(np.diff(c) <= 0), "sched is not longest-first"
 
 
+def assert_attention_close_scaled(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    """The benchmark spec's bounds for inputs that are not N(0,1): each output's error is taken
+    relative to max(1, |reference|).  Keys scaled up tile by tile make the softmax peaky,
+    so an output row is close to a single value row (|O| up to about 4.5 for N(0,1)
+    values), where the bf16 rounding of the output alone reaches half an ulp, 2^-6 =
+    0.0156, and that of P (relative 2^-9) adds to it; on N(0,1) inputs (|O| < 1 almost
+    everywhere) the bound is the plain one."""
+    o = np.asarray(o_gpu, np.float64)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    rel = np.abs(o - o_ref) / np.maximum(np.abs(o_ref), 1.0)
+    _, mean, lrel = attention_errors(o_gpu, lse_gpu, o_ref, lse_ref)
+    assert rel.max() <= MAX_ABS, f"{what}: max scaled error {rel.max():.3g} > {MAX_ABS}"
+    assert mean <= MEAN_ABS, f"{what}: mean abs {mean:.3g} > {MEAN_ABS}"
+    assert lrel <= LSE_REL, f"{what}: lse rel {lrel:.3g} > {LSE_REL}"
+    return float(rel.max()), mean, lrel
+
+
 def attention_errors(o_gpu, lse_gpu, o_ref, lse_ref):
     """Errors of GPU rows against oracle rows (same shapes, any leading layout)."""
     o = np.asarray(o_gpu, np.float64)

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import assert_attention_close, setup
+from helpers import assert_attention_close, assert_attention_close_scaled, setup
 
 pytestmark = pytest.mark.gpu
 
@@ -144,3 +144,61 @@ def test_unsupported_group_is_rejected(sift):
     with pytest.raises(sift.SiftError) as e:
         sift.dense_prefill(prob, q, k, v)
     assert e.value.code == 2
+
+
+def _rescale_events(lay, q, k, scale=None):
+    """(row, key tile) pairs of an all-ones layout at which the row's running max (log2
+    units, tiles taken in ascending order as the lists hold them) grows by more than 8:
+    the case in which the kernel rescales its O accumulator after the first tile."""
+    B = lay.tile
+    d = q.shape[-1]
+    G = q.shape[1] // k.shape[1]
+    s = (scale if scale is not None else d ** -0.5) * 1.4426950408889634
+    events = 0
+    for p in range(lay.num_prompts):
+        t0, t1 = int(lay.cu_seqlens[p]), int(lay.cu_seqlens[p + 1])
+        qp = q[t0:t1, ::G].float().cpu()           # one query head per kv head
+        kp = k[t0:t1].float().cpu()
+        sc = torch.einsum("thd,shd->hts", qp, kp) * s
+        n = t1 - t0
+        causal = torch.arange(n)[None, :] <= torch.arange(n)[:, None]
+        sc = sc.masked_fill(~causal, float("-inf"))
+        nt = (n + B - 1) // B
+        tmax = torch.stack([sc[..., j * B:(j + 1) * B].amax(-1) for j in range(nt)], -1)
+        run = tmax[..., 0]
+        for j in range(1, nt):
+            events += int(((tmax[..., j] > run + 8) & (tmax[..., j] > float("-inf"))).sum())
+            run = torch.maximum(run, tmax[..., j])
+    return events
+
+
+GROWTH = [
+    W.custom_config("att_grow_ones", [([512, 384], 128), ([256], 128)], W.BitSpec(pattern="ones"),
+                    num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128),
+    W.custom_config("att_grow_sparse", [([512, 384, 256], 128)], W.BitSpec(la_p=0.5, ca_p=0.5),
+                    num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128),
+    W.custom_config("att_grow_b64", [([256, 192], 64), ([128], 64)], W.BitSpec(la_p=0.6, ca_p=0.6),
+                    num_q_heads=4, num_kv_heads=1, head_dim=128, tile=64),
+]
+
+
+@pytest.mark.parametrize("cfg", GROWTH, ids=lambda c: c.name)
+def test_running_max_growth_matches_oracle(sift, cfg):
+    """Keys that grow in scale from tile to tile push each row's running max up by more
+    than the lazy-rescale threshold after its first tile, so the O accumulator is rescaled
+    in tensor memory mid-row (before that tile's P reaches the P*V MMA); the sparse and
+    dense kernels must still match the oracle."""
+    q, k, v = W.make_qkv(cfg, 0, device="cuda", dist="growing_keys")
+    lay, la, ca, prob, _, o, lse = _run_sparse(sift, cfg, qkv=(q, k, v))
+    if cfg.bits.pattern == "ones":
+        assert _rescale_events(lay, q, k) > 0
+    O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    assert_attention_close_scaled(o.double().cpu().numpy(), lse.double().cpu().numpy(), O, LSE,
+                           cfg.name + " sparse")
+    if cfg.bits.pattern == "ones":
+        st = prob.new_status()
+        od, lsed = sift.dense_prefill(prob, q, k, v, dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert_attention_close_scaled(od.double().cpu().numpy(), lsed.double().cpu().numpy(), O, LSE,
+                               cfg.name + " dense")

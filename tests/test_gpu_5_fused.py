@@ -11,8 +11,8 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import (assert_attention_close, gpu_rows, oracle_rows_for_pairs, sample_pairs,
-                     setup)
+from helpers import (assert_attention_close, assert_attention_close_scaled, gpu_rows,
+                     oracle_rows_for_pairs, sample_pairs, setup)
 
 pytestmark = pytest.mark.gpu
 
@@ -87,3 +87,21 @@ def test_fused_rejects_too_many_prompts(sift):
     with pytest.raises(sift.SiftError) as e:
         sift.fused_prefill(prob, 0, la_d, ca_d, q, k, v)
     assert e.value.code == 2
+
+
+def test_fused_running_max_growth(sift):
+    """Keys growing in scale tile by tile make rows rescale O mid-row; the fused kernel
+    still equals decode + sparse bit for bit and matches the oracle."""
+    cfg = W.custom_config("fu_grow", [([256] * 3, 128), ([384], 128)], W.BitSpec(la_p=0.6, ca_p=0.6),
+                          num_q_heads=4, num_kv_heads=2, head_dim=128, tile=128)
+    lay, la, ca, prob, la_d, ca_d = setup(cfg)
+    st = prob.new_status()
+    kv, cnt, sched = sift.decode(prob, la_d, ca_d, dev_status=st)
+    q, k, v = W.make_qkv(cfg, 0, device="cuda", dist="growing_keys")
+    o1, l1 = sift.sparse_prefill(prob, 0, q, k, v, kv, cnt, sched, dev_status=st)
+    o2, l2 = sift.fused_prefill(prob, 0, la_d, ca_d, q, k, v, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, sift.status_string(int(st.item()))
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    assert_attention_close_scaled(o2.double().cpu().numpy(), l2.double().cpu().numpy(), O, LSE, "fu_grow")

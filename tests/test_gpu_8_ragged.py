@@ -22,7 +22,8 @@ import torch
 
 import oracle
 import workloads as W
-from helpers import assert_attention_close, check_sched, device_bits, expand_lists
+from helpers import (assert_attention_close, assert_attention_close_scaled, check_sched,
+                     device_bits, expand_lists)
 
 pytestmark = pytest.mark.gpu
 
@@ -252,3 +253,21 @@ def test_ragged_decode_reports_a_wrong_tile_count(sift):
     assert int(st.item()) == 5  # SIFT_ERR_DEVICE_CHECK
     assert qt[NQ - 1].tolist() == [lay.total_tokens, 0]
     assert cnt[:, :, NQ - 1].eq(1).all()
+
+
+@pytest.mark.parametrize("name", ["rg_f", "rg_ones"])
+def test_ragged_running_max_growth(sift, name):
+    """General layout with keys growing in scale tile by tile (rows rescale O mid-row,
+    on gathered pages and on masked partial tiles alike) against the oracle."""
+    cfg = next(c for c in CFGS if c.name == name)
+    lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
+    qt, kv, cnt, sched, pages = _check_decode(sift, lay, la, ca, prob, la_d, ca_d)
+    st = prob.new_status()
+    q, k, v = W.make_qkv(cfg, 0, device="cuda", dist="growing_keys")
+    o, lse = sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv, cnt, sched, pages,
+                                        dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, sift.status_string(int(st.item()))
+    O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
+    assert_attention_close_scaled(o.double().cpu().numpy(), lse.double().cpu().numpy(), O, LSE,
+                           name + " growing keys")

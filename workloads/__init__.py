@@ -329,14 +329,31 @@ def make_bits(cfg: Config, layout: Layout):
     return la, ca
 
 
-def make_qkv(cfg: Config, layer: int, device="cpu", dist: str = "normal"):
-    """bf16 Q [tokens, Hq, d], K and V [tokens, Hkv, d], N(0,1) from a per-layer seed."""
+def make_qkv(cfg: Config, layer: int, device="cpu", dist: str = "normal",
+             key_growth: float = 2.5):
+    """bf16 Q [tokens, Hq, d], K and V [tokens, Hkv, d], N(0,1) from a per-layer seed.
+
+    dist="growing_keys": the same draws, but every key row is multiplied by
+    1 + key_growth * (its position inside its prompt // tile), so that a query row's
+    largest score grows from one key tile to the next (by about 4 * key_growth in log2
+    units at d = 128): inputs that make an online softmax rescale its running sums
+    after the first tile, which N(0,1) inputs almost never do.
+    """
     import torch
+    if dist not in ("normal", "growing_keys"):
+        raise ValueError(f"unknown dist {dist!r}")
     T = cfg.total_tokens
     out = []
     for name, H in (("q", cfg.num_q_heads), ("k", cfg.num_kv_heads), ("v", cfg.num_kv_heads)):
         g = torch.Generator(device=device)
         g.manual_seed(seed_for(cfg.name, layer, name))
         x = torch.randn((T, H, cfg.head_dim), generator=g, device=device, dtype=torch.float32)
+        if name == "k" and dist == "growing_keys":
+            pos = torch.empty(T, dtype=torch.int64)
+            cu = np.cumsum([0] + [sum(d) + s for d, s in cfg.prompts])
+            for p in range(len(cfg.prompts)):
+                pos[cu[p]:cu[p + 1]] = torch.arange(cu[p + 1] - cu[p])
+            f = 1.0 + key_growth * (pos // cfg.tile).to(torch.float32)
+            x = x * f.to(device).view(T, 1, 1)
         out.append(x.to(torch.bfloat16))
     return tuple(out)
