@@ -124,13 +124,40 @@ def tensor_roofline(achieved: float, kernel: str, traffic, clocks=None) -> dict:
     return r
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without its comments, whitespace runs collapsed to one space (string
+    and character literals are kept as written)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
+    """Digest of the attention kernel's code (its sources without comments or layout), so
+    that a profile summary stays matched to the code it was captured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_vector_guided_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.startswith("sift_attention") or name == "ptx.cuh":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

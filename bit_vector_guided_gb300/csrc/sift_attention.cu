@@ -27,10 +27,13 @@
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
 // P*V MMA reads it from tensor memory, so P never touches shared memory.
 // MMA order per item: S0(0) S1(0) | PV0(0) S0(1) | PV1(0) S1(1) | ... so the
-// tensor pipe works on one head while the other head's softmax runs.
+// tensor pipe works on one head while the other head's softmax runs.  Each P
+// reaches the issuer in two halves of the keys, each on a barrier of its own,
+// so P*V over the first half runs while the softmax finishes the second.
 // Online softmax keeps a per-row running max m (log2 units) and sum l; O is
 // rescaled only when m grows by more than 8 (factor 256) -- otherwise the
-// stale max is kept, which stays exact because O and l share it.
+// stale max is kept, which stays exact because O and l share it.  The rescale
+// comes before the tile's first half of P is handed over.
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA records
 // SIFT_ERR_TIMEOUT, drains its in-flight copies and MMAs, frees TMEM and
 // returns.
