@@ -12,6 +12,8 @@ computed and the rest skipped.  The configurations below are synthetic
 stand-ins with those head layouts and lengths; the batch of four prompts is
 swept over every density of the sweep (5-100%).
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -90,6 +92,18 @@ def test_qwen3_64k(sift):
     compare_decode(lay, kv, cnt, kv_o, cnt_o)
     _check_layer(sift, cfg, lay, la, ca, 0, q, k, v, o, lse, np.random.default_rng(4),
                  n_random=256)
+
+
+@pytest.mark.skipif(os.environ.get("SIFT_FULL_ORACLE") != "1",
+                    reason="about 11 TFLOP of fp64 oracle work (8 minutes on 16 host cores); "
+                           "set SIFT_FULL_ORACLE=1 to run it")
+def test_qwen3_64k_every_row(sift):
+    """The Qwen3 layer against the oracle on every (token, query head) row: 66,048 tokens
+    x 64 query heads."""
+    cfg, lay, la, ca, kv, cnt, q, k, v, o, lse = _run_single_layer(sift, "qwen3_64k")
+    assert _convex_bound_ok(o, v, cfg.num_q_heads // cfg.num_kv_heads)
+    mx, mean, lrel = _check_every_row(cfg, lay, la, ca, 0, q, k, v, o, lse)
+    print(f"qwen3_64k every row: max abs {mx:.4g}, mean abs {mean:.4g}, lse rel {lrel:.3g}")
 
 
 def test_llama_10doc_every_row(sift):
