@@ -863,20 +863,16 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                         ptx::umma_ts_c<true>(d, a + kk * 8, vb + ((kk * 16 * 128) >> 4), G::kIdescPV);
                 return true;
             };
-            // An item's last P*V pair (the "tail") completes its O.  General layout: the
-            // pattern runs on across the item boundary, each head's tail issued right before
-            // that head's first S of the next item, so that S runs while the finishing
-            // item's last softmax and epilogue do; its items are short (7 tiles on average)
-            // and it gains about 1.7%.  The aligned layout's items (16 tiles) lost about
-            // 1.4% that way, so there the tail ends its own item.
-            constexpr bool kCarry = RAGGED;
-            bool tail = false, ok = true;
-            int tail_n = 0;
-            auto issue_tail = [&]() -> bool {
-                if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, tail_n > 1))
+            // An item's last P*V pair (the "tail") completes its O; it goes out before the
+            // next item's first S.  (Issuing each head's tail right before that head's next
+            // S instead, across the item boundary, gained 1.7% on the general layout while
+            // P was handed over whole; with P in halves it lost 1.2% there, 0.3% aligned.)
+            bool ok = true;
+            auto issue_tail = [&](int n_tiles) -> bool {
+                if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, n_tiles > 1))
                     return false;
                 commit(B_(c.o_full[0]));
-                if (!issue_pv(1, vs, tail_n > 1)) return false;
+                if (!issue_pv(1, vs, n_tiles > 1)) return false;
                 commit(B_(c.o_full[1]));
                 return true;
             };
@@ -892,33 +888,22 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 if (!valid) break;
                 const uint32_t qph = qk & 1;
                 ++qk;
-                // this tile's K (and at its first tile, head 0's Q of the item)
-                auto wait_qk = [&](int j) -> bool {
-                    if (j == 0 && !wait_warp(c, B_(c.q_full[0]), qph, p)) return false;
-                    if (!wait_warp(c, B_(c.k_full[ks]), kph, p)) return false;
-                    ptx::tc_fence_after();
-                    return true;
-                };
                 for (int j = 0; j < n_tiles; ++j) {
-                    if (!kCarry && !wait_qk(j)) { ok = false; break; }
-                    // P*V of the previous tile (vs names its V): this item's, or at j = 0 the
-                    // finishing item's last, which also completes that item's O
-                    const bool pv = j > 0 || tail;
-                    const bool pv_acc = j > 0 ? j > 1 : tail_n > 1;
-                    if (pv) {
-                        if (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, pv_acc)) {
-                            ok = false;
-                            break;
-                        }
-                        if (j == 0) commit(B_(c.o_full[0]));
+                    // this tile's K (and at its first tile, head 0's Q of the item)
+                    if ((j == 0 && !wait_warp(c, B_(c.q_full[0]), qph, p)) ||
+                        !wait_warp(c, B_(c.k_full[ks]), kph, p)) {
+                        ok = false;
+                        break;
                     }
-                    if (kCarry && !wait_qk(j)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                    // P*V of the previous tile (vs names its V)
+                    if (j > 0 && (!wait_warp(c, B_(c.v_full[vs]), vph, p) || !issue_pv(0, vs, j > 1))) {
+                        ok = false;
+                        break;
+                    }
                     issue_s(0, ks);
                     commit(B_(c.s_full[0]));
-                    if (pv) {
-                        if (!issue_pv(1, vs, pv_acc)) { ok = false; break; }
-                        if (j == 0) commit(B_(c.o_full[1]));
-                    }
+                    if (j > 0 && !issue_pv(1, vs, j > 1)) { ok = false; break; }
                     if (j == 0) {  // head 1's Q of this item
                         if (!wait_warp(c, B_(c.q_full[1]), qph, p)) { ok = false; break; }
                         ptx::tc_fence_after();
@@ -929,19 +914,8 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     if (++vs == kVSlots) { vs = 0; vph ^= 1; }
                     if (++ks == kKSlots) { ks = 0; kph ^= 1; }
                 }
-                if (!ok) break;
-                tail = true;
-                tail_n = n_tiles;
-                if constexpr (!kCarry) {
-                    tail = false;
-                    if (!issue_tail()) {
-                        ok = false;
-                        break;
-                    }
-                }
+                if (!ok || !issue_tail(n_tiles)) break;
             }
-            // no item follows the last one: its tail on its own
-            if (ok && tail && __shfl_sync(kFull, c.abort, 0) == 0) (void)issue_tail();
             // every MMA issued so far must finish before TMEM and shared memory go away
             commit(B_(c.teardown));
             drain_bar(B_(c.teardown), 0, p.timeout_ns);
