@@ -16,8 +16,7 @@
 //              (general layout: straight to global memory, row by row)
 //   warps 4-7  softmax of head slot 1, the same
 //   warp  8    scheduler + K producer (K_j into a ring of 2 slots, 3 on the general
-//              layout); it claims the next item early and pulls that item's Q into L2, and
-//              runs ahead into its K tiles
+//              layout); it claims the next item early and runs ahead into its K tiles
 //   warp  9    TMEM allocator + MMA issuer (warp-wide loop, one elected lane issues)
 //   warp 10    Q + V producer (the item's Q pair once the previous one is released, then
 //              V_j into a 2-slot ring)
@@ -626,15 +625,12 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             __syncwarp();
             ++item_k;
             if (!it.valid) break;
-            // claim the following item now and pull its Q into L2 while this one runs
+            // claim the following item now, so that its tiles are known before this one
+            // ends.  (Its Q is not pulled into L2 ahead: with a whole item of K/V passing
+            // through L2 in between, 3% of the DRAM reads were such Q lines read twice.)
             int w = 0;
             if (lane == 0) w = atomicAdd(p.work_counter, 1);
             nxt = fetch(__shfl_sync(kFull, w, 0));
-            if (nxt.valid && lane == 0)
-                for (int s = 0; s < 2; ++s)
-                    for (int b = 0; b < G::kBoxes; ++b)
-                        ptx::tma_prefetch_l2_3d(&tmQ, 64 * b, nxt.hq0 + s,
-                                                RAGGED ? nxt.q0 : nxt.i * BT);
             auto load_k = [&](int idx) -> bool {
                 const int ks = kf % kKSlots;
                 if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
