@@ -40,6 +40,7 @@
 #include <cuda_bf16.h>
 
 #include <climits>
+#include <type_traits>
 #include <mutex>
 
 #include "ptx.cuh"
@@ -442,13 +443,13 @@ __device__ bool walk_bits(const AttnParams &p, const WorkItem &it, uint32_t lane
     return visit(it.i);
 }
 
-// Columns c >= lim of a key tile are cleared (to -inf), 32 at a time: a word wholly below
-// lim is left alone, one wholly at or above it is overwritten without tests, and only the
-// word that holds lim compares column by column.
-template <int BT>
+// Columns c >= lim of a key tile are cleared (to -inf) in its first NW 32-column words (the
+// words after them hide every column of the warp's rows and are not read): a word wholly
+// below lim is left alone, the others compare column by column.
+template <int BT, int NW>
 __device__ __forceinline__ void mask_from(float (&x)[BT], int lim) {
 #pragma unroll
-    for (int w = 0; w < BT / 32; ++w) {
+    for (int w = 0; w < BT / 32 && w < NW; ++w) {
         const int c0 = 32 * w;
         if (lim < c0 + 32) {
 #pragma unroll
@@ -480,17 +481,25 @@ __device__ __forceinline__ uint32_t page_word(uint32_t pm, int w, int lp) {
     return out;
 }
 
+// the row's visible columns as one limit (columns c < limit), or -1 when a page under the
+// first len columns is not kept
 template <int BT>
-__device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int row, int lp) {
+__device__ __forceinline__ int prefix_limit(uint32_t info, int row, int lp) {
     const int len = static_cast<int>(info & 0xffu);
     const bool causal = (info >> 8) & 1u;
     const uint32_t pm = info >> 16;
     const int np = min((len + (1 << lp) - 1) >> lp, BT >> lp);  // pages under [0, len)
     const uint32_t need = (1u << np) - 1u;
-    if ((pm & need) == need) {
-        mask_from<BT>(x, causal ? min(len, row + 1) : len);
-        return;
-    }
+    if ((pm & need) != need) return -1;
+    return causal ? min(len, row + 1) : len;
+}
+
+// the visibility words of a tile whose kept pages leave holes
+template <int BT>
+__device__ __forceinline__ void mask_columns(float (&x)[BT], uint32_t info, int row, int lp) {
+    const int len = static_cast<int>(info & 0xffu);
+    const bool causal = (info >> 8) & 1u;
+    const uint32_t pm = info >> 16;
 #pragma unroll
     for (int w = 0; w < BT / 32; ++w) {
         const int c0 = 32 * w;
@@ -963,74 +972,100 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     ptx::tc_fence_after();
                     float x[BT];
                     if constexpr (BT == 128) ptx::tmem_ld128(tS, x); else ptx::tmem_ld64(tS, x);
+                    // A tile whose visible columns are a prefix of each row (the diagonal; on
+                    // the general layout also partial groups and pages) is masked by a limit
+                    // per row.  On the diagonal, a warp whose rows all end in the first half
+                    // of the keys (warp-uniform) runs a copy of the code without the second
+                    // half: no max, no exponentials, P = 0 there.  (The general layout, whose
+                    // masked tiles are frequent, keeps one copy: switching between two cost
+                    // it 15% while the aligned layouts gained 1-4%.)
+                    int lim = -1;
                     if constexpr (RAGGED) {
-                        if ((info & ~kGatherBit) != p.full_info) mask_columns<BT>(x, info, row, p.lp);
-                    } else if (j == it.n - 1) {
-                        mask_from<BT>(x, row + 1);  // the diagonal tile: keys up to the row's own
-                    }
-                    // row max: independent three-input chains of 32 columns each
-                    float mxc[BT / 32];
-#pragma unroll
-                    for (int q = 0; q < BT / 32; ++q) {
-                        const float *xb = x + 32 * q;
-                        float a = ptx::fmax3(xb[0], xb[1], xb[2]);
-#pragma unroll
-                        for (int t = 3; t < 31; t += 2) a = ptx::fmax3(a, xb[t], xb[t + 1]);
-                        mxc[q] = fmaxf(a, xb[31]);
-                    }
-                    float mx = fmaxf(mxc[0], mxc[1]);
-                    if constexpr (BT == 128) mx = ptx::fmax3(mx, mxc[2], mxc[3]);
-                    const float m_new = fmaxf(m, mx * sl2);
-                    const bool need = m_new > m + 8.0f;
-                    float alpha = 1.f;
-                    if (need) {
-                        alpha = ptx::ex2(m - m_new);
-                        m = m_new;
-                    }
-                    // p = 2^(x*scale*log2e - m): packed FMA, MUFU ex2, packed partial sums.
-                    // Each half of the keys is handed to the MMA issuer as soon as it is stored.
-                    const uint64_t sl2x2 = ptx::f2(sl2, sl2);
-                    const uint64_t nmb = ptx::f2(-m, -m);
-                    uint64_t acc[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) acc[q] = ptx::f2(0.f, 0.f);
-                    uint32_t pk[BT / 2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-                        for (int t = h * (BT / 4); t < (h + 1) * (BT / 4); ++t) {
-                            float e0, e1;
-                            ptx::f2_split(ptx::ffma2(ptx::f2(x[2 * t], x[2 * t + 1]), sl2x2, nmb), e0, e1);
-                            const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
-                            acc[t & 3] = ptx::fadd2(acc[t & 3], ptx::f2(p0, p1));
-                            pk[t] = ptx::pack_bf16x2(p0, p1);
+                        if ((info & ~kGatherBit) != p.full_info) {
+                            lim = prefix_limit<BT>(info, row, p.lp);
+                            if (lim < 0) mask_columns<BT>(x, info, row, p.lp);
                         }
-                        const uint32_t(&half)[BT / 4] =
-                            *reinterpret_cast<const uint32_t(*)[BT / 4]>(pk + h * (BT / 4));
-                        if constexpr (BT == 128) ptx::tmem_st32(tS + h * 32, half);
-                        else ptx::tmem_st16(tS + h * 16, half);
-                        // O takes the new max before any of this tile's P reaches the tensor
-                        // pipe (this head's P*V of the previous tile finished before its S did)
-                        if (h == 0 && j > 0 && __any_sync(kFull, need)) {
-#pragma unroll 1
-                            for (int cc = 0; cc < HD / 32; ++cc) {
-                                float ov[32];
-                                ptx::tmem_ld32(tO + cc * 32, ov);
+                    } else if (j == it.n - 1) {
+                        lim = row + 1;  // the diagonal tile: keys up to the row's own
+                    }
+                    int nw = BT / 32;  // leading 32-column words visible to some row of the warp
+                    if (!RAGGED && lim >= 0)  // uniform: the diagonal tile, for the whole warp
+                        nw = (__reduce_max_sync(kFull, static_cast<unsigned>(lim)) + 31) >> 5;
+                    auto tile = [&](auto nw_c) {
+                        constexpr int NW = decltype(nw_c)::value;
+                        if (lim >= 0) mask_from<BT, NW>(x, lim);
+                        // row max: independent three-input chains of 32 columns each
+                        float mxc[BT / 32];
 #pragma unroll
-                                for (int t = 0; t < 32; ++t) ov[t] *= alpha;
-                                ptx::tmem_st32f(tO + cc * 32, ov);
+                        for (int q = 0; q < BT / 32; ++q) {
+                            mxc[q] = -INFINITY;
+                            if (q < NW) {
+                                const float *xb = x + 32 * q;
+                                float a = ptx::fmax3(xb[0], xb[1], xb[2]);
+#pragma unroll
+                                for (int t = 3; t < 31; t += 2) a = ptx::fmax3(a, xb[t], xb[t + 1]);
+                                mxc[q] = fmaxf(a, xb[31]);
                             }
                         }
-                        ptx::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(B_(h == 0 ? c.p_half[s] : c.p_full[s]));
-                    }
-                    {
+                        float mx = fmaxf(mxc[0], mxc[1]);
+                        if constexpr (BT == 128) mx = ptx::fmax3(mx, mxc[2], mxc[3]);
+                        const float m_new = fmaxf(m, mx * sl2);
+                        const bool need = m_new > m + 8.0f;
+                        float alpha = 1.f;
+                        if (need) {
+                            alpha = ptx::ex2(m - m_new);
+                            m = m_new;
+                        }
+                        // p = 2^(x*scale*log2e - m): packed FMA, MUFU ex2, packed partial sums.
+                        // Each half of the keys goes to the MMA issuer as soon as it is stored.
+                        const uint64_t sl2x2 = ptx::f2(sl2, sl2);
+                        const uint64_t nmb = ptx::f2(-m, -m);
+                        uint64_t acc[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) acc[q] = ptx::f2(0.f, 0.f);
+                        uint32_t pk[BT / 2];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                            for (int t = h * (BT / 4); t < (h + 1) * (BT / 4); ++t) {
+                                if (t < 16 * NW) {
+                                    float e0, e1;
+                                    ptx::f2_split(ptx::ffma2(ptx::f2(x[2 * t], x[2 * t + 1]), sl2x2, nmb),
+                                                  e0, e1);
+                                    const float p0 = ptx::ex2(e0), p1 = ptx::ex2(e1);
+                                    acc[t & 3] = ptx::fadd2(acc[t & 3], ptx::f2(p0, p1));
+                                    pk[t] = ptx::pack_bf16x2(p0, p1);
+                                } else {
+                                    pk[t] = 0u;
+                                }
+                            }
+                            const uint32_t(&half)[BT / 4] =
+                                *reinterpret_cast<const uint32_t(*)[BT / 4]>(pk + h * (BT / 4));
+                            if constexpr (BT == 128) ptx::tmem_st32(tS + h * 32, half);
+                            else ptx::tmem_st16(tS + h * 16, half);
+                            // O takes the new max before any of this tile's P reaches the tensor
+                            // pipe (this head's P*V of the previous tile finished before its S did)
+                            if (h == 0 && j > 0 && __any_sync(kFull, need)) {
+#pragma unroll 1
+                                for (int cc = 0; cc < HD / 32; ++cc) {
+                                    float ov[32];
+                                    ptx::tmem_ld32(tO + cc * 32, ov);
+#pragma unroll
+                                    for (int t = 0; t < 32; ++t) ov[t] *= alpha;
+                                    ptx::tmem_st32f(tO + cc * 32, ov);
+                                }
+                            }
+                            ptx::tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) ptx::mbar_arrive(B_(h == 0 ? c.p_half[s] : c.p_full[s]));
+                        }
                         float a0, a1;
                         ptx::f2_split(ptx::fadd2(ptx::fadd2(acc[0], acc[1]), ptx::fadd2(acc[2], acc[3])),
                                       a0, a1);
                         l = l * alpha + (a0 + a1);
-                    }
+                    };
+                    if (!RAGGED && nw <= BT / 64) tile(std::integral_constant<int, BT / 64>{});
+                    else tile(std::integral_constant<int, BT / 32>{});
                 }
                 if (!ok) break;
                 if (!wait_warp(c, B_(c.o_full[s]), oph, p)) break;
