@@ -691,6 +691,8 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
             "link_floor_ms_per_step": 1e3 * floor,
             "link_fastest_ms_per_step": 1e3 * floor_min,
             "link_mean_ms_per_step": 1e3 * floor_mean,
+            "link_reps_ms": [round(1e3 * r, 2) for r in reps],
+            "ratio_to_link_mean": (el / steps) / floor_mean,
             "link_gbs": (h2d + d2h) / floor / 1e9,
             "ratio_to_link_floor": (el / steps) / floor,
             "note": "pinned host buffers; H2D of each layer's Q/K/V on one copy stream and "
@@ -699,7 +701,8 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
                     "link_floor_ms_per_step: the same copies alone on the same streams, "
                     "both directions at once, no kernels: the median of 10 repetitions "
                     "timed just before and after the e2e steps (link_fastest / link_mean: "
-                    "their fastest and their mean)"}
+                    "their fastest and their mean; link_reps_ms: each of them, since the "
+                    "link's speed can switch between states during a run)"}
 
 
 def run_sweep(args, dev, stream):

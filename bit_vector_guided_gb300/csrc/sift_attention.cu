@@ -61,6 +61,7 @@ constexpr int kStoreWarp = 11;     // TMA stores of O
 // keep the copy engine busier, the TMA stores cost 5%).  V ring: two slots.
 constexpr int kKSlotsMax = 3;
 constexpr int kVSlots = 2;
+constexpr int kRing = 16;  // key tiles in flight from the K producer to the V producer (bits)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kMinSmem = 120 * 1024;  // forces one CTA per SM (the CTA owns all of TMEM)
@@ -104,6 +105,11 @@ struct Ctl {
     uint64_t stage_full[2], stage_free[2];
     uint64_t sch_full[2], sch_empty[2];
     uint64_t teardown, never;
+    // rows walked from the bits: the K producer hands each key tile it finds to the V
+    // producer (entry t % kRing of tile t, complete once written); the V producer trails
+    // by a few tiles at most, since S(j) is issued only after V(j-1) has landed
+    uint64_t ring_full[kRing];
+    int32_t ring[kRing];
     WorkItem items[2];
     uint32_t tmem_base;
     volatile int32_t abort;
@@ -156,14 +162,14 @@ struct Geo {
     static constexpr int kOBox = BT * 128;                 // bytes: tile rows x 128 B
     static constexpr int kOOff = kVOff + kVSlots * kKVBytes;  // O staging tile, kBoxes boxes
     static constexpr int kCtlOff = kOOff + (STAGED ? kBoxes * kOBox : 0);
-    static constexpr int kSmemUsed = kCtlOff + 1024 + 1024;  // + control block + align slack
+    static constexpr int kSmemUsed = kCtlOff + 1536 + 1024;  // + control block + align slack
     static constexpr int kSmem = kSmemUsed > kMinSmem ? kSmemUsed : kMinSmem;
     static constexpr uint32_t kTxQ = 2 * kBoxes * BT * 128;
     static constexpr uint32_t kTxKV = kBoxes * BT * 128;
     static constexpr int kSoftWarps = BT / 32;       // active softmax warps per head slot
     static constexpr uint32_t kIdescS = ptx::idesc_bf16(128, BT, false, false);
     static constexpr uint32_t kIdescPV = ptx::idesc_bf16(128, HD, false, true);
-    static_assert(sizeof(Ctl) <= 1024, "control block");
+    static_assert(sizeof(Ctl) <= 1536, "control block");
     static_assert(kSmemUsed <= 227 * 1024, "shared memory");
 };
 
@@ -574,6 +580,7 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             ptx::mbar_init(B_(c.stage_free[s]), 1);
         }
         ptx::mbar_init(B_(c.teardown), 1);
+        for (int r = 0; r < kRing; ++r) ptx::mbar_init(B_(c.ring_full[r]), 1);
         ptx::mbar_init(B_(c.never), 1);
         c.abort = 0;
         if (MODE == kModeBits) {
@@ -681,7 +688,13 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 return true;
             };
             if constexpr (MODE == kModeBits) {
-                alive = walk_bits(p, it, lane, load_k);
+                alive = walk_bits(p, it, lane, [&](int idx) -> bool {
+                    if (lane == 0) {  // published before the load, for the V producer
+                        c.ring[kf % kRing] = idx;
+                        ptx::mbar_arrive(B_(c.ring_full[kf % kRing]));
+                    }
+                    return load_k(idx);
+                });
             } else if constexpr (RAGGED) {
                 for (int jb = 0; jb < it.n && alive; jb += 32) {
                     const int2 e = ragged_entry(p, it, jb + static_cast<int>(lane));
@@ -773,7 +786,15 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 return true;
             };
             if constexpr (MODE == kModeBits) {
-                alive = walk_bits(p, it, lane, load_v);
+                // the K producer's tiles, in the same order (it walked the bits once)
+                for (int j = 0; j < it.n && alive; ++j) {
+                    const int r = vf % kRing;
+                    if (!wait_warp(c, B_(c.ring_full[r]), (vf / kRing) & 1, p)) {
+                        alive = false;
+                        break;
+                    }
+                    alive = load_v(c.ring[r]);
+                }
             } else if constexpr (RAGGED) {
                 for (int jb = 0; jb < it.n && alive; jb += 32) {
                     const int2 e = ragged_entry(p, it, jb + static_cast<int>(lane));
