@@ -10,7 +10,8 @@
 //
 // One work item = (query tile i, kv head h, pair of query heads of h's group).
 // Both heads of the pair share every K/V tile staged in shared memory, and the
-// decoded list of row (h, i).  Roles inside the 384-thread CTA:
+// decoded list of row (h, i).  Roles inside the CTA (384 threads; 352 on the general
+// layout, which has no warp 11):
 //   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane); after the item's
 //              last tile, its epilogue: O / l in bf16 into the shared-memory staging tile
 //              (general layout: straight to global memory, row by row)
@@ -19,9 +20,10 @@
 //              layout); it claims the next item early and runs ahead into its K tiles
 //   warp  9    TMEM allocator + MMA issuer (warp-wide loop, one elected lane issues)
 //   warp 10    Q + V producer (the item's Q pair once the previous one is released, then
-//              V_j into a 2-slot ring)
+//              V_j into a 2-slot ring; for rows walked from the bits it takes warp 8's
+//              tile coordinates from a shared-memory ring instead of walking them again)
 //   warp 11    O writer: one TMA store per staged head tile, then hands the staging tile
-//              back once the store has read it (idle on the general layout)
+//              back once the store has read it
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
 // P*V MMA reads it from tensor memory, so P never touches shared memory.
