@@ -471,18 +471,30 @@ def run_ours(args, cfg):
 
     traffic = None if shard else profiled_traffic(profile_summary(cfg.name), cfg.name)
 
-    # decode fused into the prefill: the same step without a separate decode
-    fz0, fz1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    for rep in range(2):
-        if rep == 1:
-            fz0.record(stream)
+    # decode fused into the prefill: the same step without a separate decode, timed over
+    # as many steps as the main measurement and alternating with decode + sparse steps
+    # (the GPU's speed drifts by a few percent within a run, so the two are compared
+    # side by side rather than minutes apart)
+    def fused_step():
         for l in range(L):
             q, k, v = qkv[l]
             o, lse = outs[l]
             sift.fused_prefill(prob, l, la_d, ca_d, q, k, v, 0.0, o, lse, ws, status, stream)
-    fz1.record(stream)
-    torch.cuda.synchronize(dev)
-    fused_ms_step = fz0.elapsed_time(fz1)
+
+    fused_step()
+    pair_ms = {"fused": [], "decoded": []}
+    for _ in range(max(3, min(args.steps, 10))):
+        for name, fn in (("fused", fused_step), ("decoded", step)):
+            fz0, fz1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            fz0.record(stream)
+            fn()
+            fz1.record(stream)
+            torch.cuda.synchronize(dev)
+            pair_ms[name].append(fz0.elapsed_time(fz1))
+    if int(status.item()) != 0:
+        raise RuntimeError("device status " + sift.status_string(int(status.item())))
+    fused_ms_step = float(np.mean(pair_ms["fused"]))
+    fused_vs_decoded = fused_ms_step / float(np.mean(pair_ms["decoded"]))
 
     # offline bit builder (one layer), outside the timed region: into scratch words
     max_doc_tiles = max([(int(lay.doc_end[g]) - lay.doc_start(g)) // cfg.tile
@@ -546,6 +558,7 @@ def run_ours(args, cfg):
         # diagonal tiles counted at the (B+1)/(2B) of their entries that are causal
         "useful_tflops": value * useful_fraction(cfg, lay, flops_step),
         "fused_ms_per_step": fused_ms_step,
+        "fused_vs_decoded": fused_vs_decoded,
         "fused_ms_per_layer": fused_ms_step / L,
         "fused_tflops": flops_step / (fused_ms_step * 1e-3) / 1e12,
         "decode_launches_per_step": decode_launches(lay),
