@@ -644,11 +644,28 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             ++item_k;
             if (!it.valid) break;
             // claim the following item now, so that its tiles are known before this one
-            // ends.  (Its Q is not pulled into L2 ahead: with a whole item of K/V passing
-            // through L2 in between, 3% of the DRAM reads were such Q lines read twice.)
+            // ends.  On decoded lists and dense rows longer than the K ring, its schedule
+            // entry and count (dependent loads) are read only once this item's first K
+            // tiles fill the ring, where they no longer hold back its first tile (aligned
+            // 1-2% faster).  Elsewhere they are read at once: after a short row the next
+            // item would wait for them, and on the general layout and on rows walked from
+            // the bits the late read measured 1-7% slower.  (The next item's Q is not
+            // pulled into L2 ahead: with a whole item of K/V passing through L2 in between,
+            // 3% of the DRAM reads were such Q lines read twice.)
             int w = 0;
             if (lane == 0) w = atomicAdd(p.work_counter, 1);
-            nxt = fetch(__shfl_sync(kFull, w, 0));
+            w = __shfl_sync(kFull, w, 0);
+            constexpr bool kLateFetch = MODE == kModeList || MODE == kModeDense;
+            bool fetched = !(kLateFetch && it.n > kKSlots);
+            if (fetched) nxt = fetch(w);
+            int k_in_item = 0;
+            auto after_k = [&](bool ok) -> bool {
+                if (ok && !fetched && ++k_in_item == kKSlots) {
+                    nxt = fetch(w);
+                    fetched = true;
+                }
+                return ok;
+            };
             auto load_k = [&](int idx) -> bool {
                 const int ks = kf % kKSlots;
                 if (!wait_warp(c, B_(c.k_empty[ks]), ((kf / kKSlots) & 1) ^ 1, p)) return false;
@@ -712,9 +729,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     const int idx_l = list_entry<MODE>(p, it, jb + static_cast<int>(lane));
                     const int cnt = min(32, it.n - jb);
                     for (int jj = 0; jj < cnt && alive; ++jj)
-                        alive = load_k(__shfl_sync(kFull, idx_l, jj));
+                        alive = after_k(load_k(__shfl_sync(kFull, idx_l, jj)));
                 }
             }
+            if (!fetched) nxt = fetch(w);
         }
         if (c.abort && lane == 0) {
             // unwinding: let every copy already issued land before shared memory is released
