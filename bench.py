@@ -678,15 +678,19 @@ def run_e2e(args, cfg, lay, prob, la, ca, qkv, outs, kv_idx, counts, sched, stat
             out.append(time.perf_counter() - t1)
         return out
 
-    for _ in range(max(1, min(args.warmup, 2))):
-        step()
-    copies_only()
-    torch.cuda.synchronize(dev)
     steps = max(1, min(args.steps, 5))
     # The link's speed swings from moment to moment on a shared host (copy repetitions of
-    # one run have differed by 40%), so the floor is the median of repetitions timed just
-    # before and just after the e2e steps; their fastest and their mean are reported too.
+    # one run have differed by 40%), so the floor is the median of repetitions timed before
+    # and just after the e2e steps; their fastest and their mean are reported too.  The
+    # first copy-only repetition after kernels ran, and the first step with kernels after
+    # copy-only traffic, each took about 130 ms longer than the rest, so the e2e warm-up
+    # steps run after the copy-only repetitions, directly before the timed steps.
+    copies_only()
+    torch.cuda.synchronize(dev)
     reps = copy_reps(5)
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize(dev)
     if dist is not None:
         dist.barrier()
     t0 = time.perf_counter()

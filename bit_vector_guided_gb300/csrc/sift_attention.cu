@@ -102,8 +102,9 @@ struct Ctl {
     uint64_t k_full[kKSlotsMax], k_empty[kKSlotsMax], v_full[kVSlots], v_empty[kVSlots];
     // p_half[s]: the first half of head s's P (keys [0, B/2)) is in tensor memory
     uint64_t s_full[2], p_half[2], p_full[2], o_full[2];
-    // the O staging tile, used by head 0 and head 1 in turn: stage_full[s] when head s has
-    // written it, stage_free[s] when the TMA store of head s's tile has read it
+    // O staging: head 0 writes the staging tile, head 1 the V ring slot of the item's last
+    // V tile; stage_full[s] when head s has written its tile, stage_free[0] when the TMA
+    // store of head 0's tile has read it (head 1's slot goes back through v_empty)
     uint64_t stage_full[2], stage_free[2];
     uint64_t sch_full[2], sch_empty[2];
     uint64_t teardown, never;
@@ -1111,22 +1112,23 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 if (!ok) break;
                 if (!wait_warp(c, B_(c.o_full[s]), oph, p)) break;
                 oph ^= 1;
-                if (releaser) ptx::mbar_arrive(B_(c.v_empty[(t + kVSlots - 1) % kVSlots]));
+                // the item's last V slot: head 1 stages its O there on staged layouts (the
+                // O writer hands the slot back once the store has read it)
+                const int last_vslot = (t + kVSlots - 1) % kVSlots;
+                if (releaser && !STAGED) ptx::mbar_arrive(B_(c.v_empty[last_vslot]));
                 ptx::tc_fence_after();
-                // Aligned tiles go through the staging tile and one TMA store per box; the
-                // general layout's tiles are written row by row (a partial one must not spill
-                // into the next segment, and the stores would compete with its gathered page
-                // loads).  The heads take the staging tile in turn: head 0's m-th tile after
-                // head 1's (m-1)-th has been read, head 1's after head 0's m-th.
+                // Aligned tiles are staged in shared memory and go out as one TMA store per
+                // box; the general layout's tiles are written row by row (a partial one must
+                // not spill into the next segment, and the stores would compete with its
+                // gathered page loads).  Head 0 stages in the staging tile, once the store of
+                // its previous tile has read it; head 1 in the slot of the item's last V tile,
+                // free as soon as P*V is done (o_full).  (When both heads took the staging
+                // tile in turn, head 1's epilogue waited for head 0's store: 2,970 cycles
+                // against head 0's 1,120, which held back head 1's next softmax.)
                 const bool staged = STAGED;
-                if (staged) {
-                    bool free_ok = true;
-                    if (s == 0 && n_staged > 0)
-                        free_ok = wait_warp(c, B_(c.stage_free[1]), (n_staged - 1) & 1, p);
-                    else if (s == 1)
-                        free_ok = wait_warp(c, B_(c.stage_free[0]), n_staged & 1, p);
-                    if (!free_ok) break;
-                }
+                if (staged && s == 0 && n_staged > 0 &&
+                    !wait_warp(c, B_(c.stage_free[0]), (n_staged - 1) & 1, p))
+                    break;
                 const float inv = 1.f / l;
                 const int64_t tok = RAGGED ? static_cast<int64_t>(it.q0) + row
                                            : static_cast<int64_t>(it.i) * BT + row;
@@ -1137,7 +1139,9 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                 const bool store = !RAGGED || row < it.qlen;
                 // this row in the staging tile: box cc/2, 128 bytes per row, 16-byte chunks
                 // placed by the 128-byte swizzle (chunk k of row r at k ^ (r % 8))
-                const uint32_t srow = o_s + static_cast<uint32_t>(row) * 128u;
+                const uint32_t srow =
+                    (s == 0 ? o_s : v_s + static_cast<uint32_t>(last_vslot) * G::kKVBytes) +
+                    static_cast<uint32_t>(row) * 128u;
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     float ov[32];
@@ -1181,9 +1185,10 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
     } else if (STAGED && warp == kStoreWarp) {
         // ------------------------------------------------ O writer
         // Follows the items; for each whole tile, head 0's then head 1's staged O goes out
-        // as one TMA store per 64-column box (one lane per box), and the staging tile is
-        // handed back once the store has read it.
-        int item_k = 0, n = 0;
+        // as one TMA store per 64-column box (one lane per box).  Once a store has read its
+        // tile, head 0's staging tile goes back to head 0 and head 1's (the item's last V
+        // slot) to the V producer.
+        int item_k = 0, n = 0, t = 0;
         bool issued = false;
         while (true) {
             const int slot = item_k & 1;
@@ -1194,20 +1199,24 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
             ++item_k;
             if (!it.valid) break;
             const int tok0 = RAGGED ? it.q0 : it.i * BT;
+            t += it.n;
+            const int last_vslot = (t + kVSlots - 1) % kVSlots;
             bool ok = true;
             for (int s = 0; s < 2; ++s) {
                 if (!wait_warp(c, B_(c.stage_full[s]), n & 1, p)) {
                     ok = false;
                     break;
                 }
+                const uint32_t src =
+                    s == 0 ? o_s : v_s + static_cast<uint32_t>(last_vslot) * G::kKVBytes;
                 if (static_cast<int>(lane) < G::kBoxes) {
-                    ptx::tma_store_3d(&tmO, o_s + lane * G::kOBox, 64 * lane, it.hq0 + s, tok0);
+                    ptx::tma_store_3d(&tmO, src + lane * G::kOBox, 64 * lane, it.hq0 + s, tok0);
                     ptx::bulk_commit();
                     ptx::bulk_wait_read();
                     issued = true;
                 }
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(B_(c.stage_free[s]));
+                if (lane == 0) ptx::mbar_arrive(B_(s == 0 ? c.stage_free[0] : c.v_empty[last_vslot]));
             }
             if (!ok) break;
             ++n;
