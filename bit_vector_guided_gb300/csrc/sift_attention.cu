@@ -15,7 +15,8 @@
 //   warps 0-3  softmax of head slot 0 (thread = query row = TMEM lane); after the item's
 //              last tile, its epilogue: O / l in bf16 into the shared-memory staging tile
 //              (general layout: straight to global memory, row by row)
-//   warps 4-7  softmax of head slot 1, the same
+//   warps 4-7  softmax of head slot 1, the same, staging into the V ring slot of the
+//              item's last V tile instead (free once P*V is done)
 //   warp  8    scheduler + K producer (K_j into a ring of 2 slots, 3 on the general
 //              layout); it claims the next item early and runs ahead into its K tiles
 //   warp  9    TMEM allocator + MMA issuer (warp-wide loop, one elected lane issues)
@@ -23,7 +24,7 @@
 //              V_j into a 2-slot ring; for rows walked from the bits it takes warp 8's
 //              tile coordinates from a shared-memory ring instead of walking them again)
 //   warp 11    O writer: one TMA store per staged head tile, then hands the staging tile
-//              back once the store has read it
+//              back to head 0, and the V slot to the V producer, once the store has read it
 // Tensor memory (128 lanes x 512 columns): S_0 | S_1 | O_0 | O_1, 128 columns
 // each.  P (bf16, two per column) overwrites the first half of its S, and the
 // P*V MMA reads it from tensor memory, so P never touches shared memory.
