@@ -1026,7 +1026,18 @@ sift_attention_kernel(const __grid_constant__ CUtensorMap tmQ,
                     if constexpr (RAGGED) {
                         if ((info & ~kGatherBit) != p.full_info) {
                             lim = prefix_limit<BT>(info, row, p.lp);
-                            if (lim < 0) mask_columns<BT>(x, info, row, p.lp);
+                            // Pages whose kept bits leave holes in a tile come only from
+                            // 4-token pages under 64-token tiles (larger pages below the
+                            // tile are gathered, and pages of a tile or more are one bit).
+                            // The 128-token kernel leaves that code out (2% on its general
+                            // layout) and reports such an entry, read as its first len keys.
+                            if constexpr (BT == 64) {
+                                if (lim < 0) mask_columns<BT>(x, info, row, p.lp);
+                            } else if (lim < 0) {
+                                set_status(p.status, SIFT_ERR_DEVICE_CHECK);
+                                lim = static_cast<int>(info & 0xffu);
+                                if ((info >> 8) & 1u) lim = min(lim, row + 1);
+                            }
                         }
                     } else if (j == it.n - 1) {
                         lim = row + 1;  // the diagonal tile: keys up to the row's own

@@ -326,6 +326,10 @@ sift_status sift_decode_ragged(const sift_problem *prob, int32_t num_query_tiles
  * rows of each query tile inside its segment are written.  Gathered pages
  * are loaded by TMA page rows at a time side by side into one key tile.
  * qtiles, kv, counts, sched, pages, page_cap: as from sift_decode_ragged.
+ * With 128-token tiles every entry sift_decode_ragged writes leaves its visible
+ * keys a prefix of each row (kept pages with holes between them arise only from
+ * 4-token pages under 64-token tiles); an entry whose mask leaves holes is read
+ * there as its first len keys and reported as SIFT_ERR_DEVICE_CHECK.
  * One memset and one kernel launch.
  */
 sift_status sift_sparse_prefill_ragged(const sift_problem *prob, int32_t num_query_tiles,
