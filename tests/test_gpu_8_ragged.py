@@ -271,3 +271,33 @@ def test_ragged_running_max_growth(sift, name):
     O, LSE = oracle.attention_all(lay, la, ca, 0, q, k, v)
     assert_attention_close_scaled(o.double().cpu().numpy(), lse.double().cpu().numpy(), O, LSE,
                            name + " growing keys")
+
+
+def test_hole_entry_with_128_token_tiles_is_reported(sift):
+    """With 128-token tiles the decode writes only entries whose visible keys form a prefix
+    of each row (pages below the tile are gathered); an entry whose page mask leaves a hole
+    is read there as its first len keys and reported as a device check."""
+    cfg = next(c for c in CFGS if c.name == "rg_ones")
+    assert cfg.tile == 128 and cfg.page < cfg.tile
+    lay, la, ca, prob, la_d, ca_d = _setup(sift, cfg)
+    qt, kv, cnt, sched, pages = sift.decode_ragged(prob, la_d, ca_d)
+    torch.cuda.synchronize()
+    q, k, v = W.make_qkv(cfg, 0, device="cuda")
+    st = prob.new_status()
+    o_ok, l_ok = sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv, cnt, sched, pages,
+                                            dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # the first query tile's only entry is its own tile: drop the first page's bit
+    assert int(cnt[0, 0, 0]) == 1
+    info = int(kv[0, 0, 0, 0, 1])
+    assert info & (1 << 8) and (info >> 16) & 1
+    kv_bad = kv.clone()
+    kv_bad[0, 0, 0, 0, 1] = info & ~(1 << 16)
+    st = prob.new_status()
+    o, l = sift.sparse_prefill_ragged(prob, 0, q, k, v, qt, kv_bad, cnt, sched, pages,
+                                      dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 5, sift.status_string(int(st.item()))  # SIFT_ERR_DEVICE_CHECK
+    assert torch.isfinite(o.float()).all() and torch.isfinite(l).all()
+    assert torch.equal(o, o_ok) and torch.equal(l, l_ok)  # read as its first len keys
